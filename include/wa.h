@@ -1,0 +1,130 @@
+/*
+ * wa.h — sliding-window grouped-query attention on one GB300 (sm_103a).
+ *
+ * Plain C ABI: device pointers, host scalars, one CUDA stream handle passed
+ * as void*.  No call allocates, frees or synchronizes, except wa_status,
+ * which reads the status word back and therefore waits for the stream.
+ *
+ * The operation, as defined by TensorFold pull request #1123 ("window_attention
+ * at head dim 256"), section "What this changes":
+ *
+ *   o[row, h] = softmax(scale * q[row, h] . K^T) V  over the row's visible keys,
+ *
+ * where query head h reads key head g = h / G (G = hq / hkv, at most 16), the
+ * key at absolute position j lives in ring slot j mod ring, and the visible
+ * keys are [lo, last] with lo = max(0, p - win + 1) for win > 0 and lo = 0 for
+ * win = 0 (a linear cache whose ring is its length).  Probabilities stay fp32;
+ * the output is bf16, round to nearest even.  Any (row, head) whose output is
+ * NaN or infinite is recomputed in float64 (bullet "A NaN or infinite output
+ * re-runs its head in float64"), so non-finite outputs carry float64's class.
+ *
+ * bf16 tensors are passed as raw 16-bit storage (const void*).  Every tensor
+ * base pointer must be 16-byte aligned, and every token stride a multiple of
+ * 8 elements.  A row's output bits depend only on that row's inputs: not on
+ * the batch around it, its slot in the batch, the declared cache length, or
+ * how a prompt is cut into chunks.
+ *
+ * Return codes: WA_OK (0) or a negative WA_E* code.  Argument errors are
+ * reported before anything is enqueued.  Errors that only the device can see
+ * (a bad pos or hi value in device memory, a wait that ran out) are clamped
+ * for memory safety and reported as WA_STATUS_* bits through wa_status.
+ */
+#ifndef WA_H
+#define WA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WA_OK 0
+#define WA_EINVAL (-1)        /* an argument is outside the supported set */
+#define WA_EWORKSPACE (-2)    /* ws is null, misaligned or smaller than the *_ws_bytes query */
+#define WA_ECUDA (-3)         /* a CUDA call or launch failed */
+#define WA_EDEVICE (-4)       /* the current device is not a compute capability 10.3 GPU */
+
+#define WA_STATUS_BAD_POS 1   /* a decode pos was < 0, or >= ring with win = 0 (clamped) */
+#define WA_STATUS_BAD_HI 2    /* a prompt hi[i] was outside [p0+i, p0+n-1] (clamped) */
+#define WA_STATUS_TIMEOUT 4   /* a bounded device wait gave up; outputs are not valid */
+
+/* Token strides in elements for the prompt form (head stride is always d).
+ * Zero means dense: hq*d for q and out, hkv*d for k and v. */
+typedef struct wa_strides {
+    int64_t q;
+    int64_t k;
+    int64_t v;
+    int64_t out;
+} wa_strides;
+
+/* Workspace bytes wa_decode needs for these sizes: a 256-byte header (status
+ * word, re-run list), one int32 re-run slot per (row, head), and one fp32
+ * partial (m, l, o[d]) per (row, head, 256-key chunk).  0 for invalid sizes. */
+size_t wa_decode_ws_bytes(int32_t rows, int32_t hq, int32_t d, int32_t win, int32_t ring);
+
+/*
+ * Decode form (bullet "Decode" of "What this changes"): few rows, long cache.
+ *
+ *   q      [rows, hq, d]         bf16, dense
+ *   k_ring [rows, ring, hkv, d]  bf16, dense; row r owns ring k_ring[r]
+ *   v_ring [rows, ring, hkv, d]  bf16, dense
+ *   pos    [rows]                int32, device; row r's last key position p
+ *   out    [rows, hq, d]         bf16, written
+ *   ws     wa_decode_ws_bytes(...) bytes of device memory, 256-byte aligned
+ *
+ * Keys are processed in 256-key chunks at absolute positions [256c, 256c+255];
+ * one CTA per (chunk, key head, row) writes the chunk's (m, l, o) in fp32, and
+ * a second kernel merges the chunks in chunk order:
+ * o = sum_c a_c o_c / sum_c a_c l_c with a_c = exp(m_c - M).
+ * d is 128 or 256; hq % hkv == 0 and hq / hkv <= 16; 0 <= win <= ring; win = 0
+ * needs pos < ring.  Returns WA_EINVAL otherwise.
+ */
+int wa_decode(const void* q, const void* k_ring, const void* v_ring, const int32_t* pos,
+              int32_t rows, int32_t hq, int32_t hkv, int32_t d, int32_t win, int32_t ring,
+              float scale, void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes wa_prompt needs: the 256-byte header and one int32 re-run
+ * slot per (row, head).  0 for invalid sizes. */
+size_t wa_prompt_ws_bytes(int32_t n, int32_t hq);
+
+/*
+ * Prompt form (bullets "Prompt", "Window.p32" and "promptRows(..., hi)"):
+ * n rows at positions p0 .. p0+n-1 of one sequence.
+ *
+ *   q    [n, hq, d]      bf16, token stride strides->q (default hq*d)
+ *   k    [ring, hkv, d]  bf16, token stride strides->k (default hkv*d); the
+ *                        chunk's own keys are already in the ring
+ *   v    [ring, hkv, d]  bf16, token stride strides->v (default hkv*d)
+ *   hi   [n] int32, device, or NULL: row i sees keys [lo_i, hi[i]] with
+ *        p0+i <= hi[i] <= p0+n-1; NULL means hi[i] = p0+i (causal)
+ *   p32  0: P enters P.V as one bf16; 1: as bf16(P) + bf16(P - bf16(P))
+ *   out  [n, hq, d]      bf16, token stride strides->out (default hq*d)
+ *
+ * Tensor-core tiles (tcgen05, accumulators in tensor memory, operands staged
+ * by TMA) over 128-row query tiles and key tiles at absolute positions, with
+ * an fp32 online softmax.  Constraints: d in {128, 256}; hq % hkv == 0 and
+ * hq / hkv <= 16; n >= 1, p0 >= 0; for win > 0, win <= ring and the chunk
+ * plus its window fits the ring (p0+n-1 - max(0, p0-win+1) < ring); for
+ * win = 0, p0 + n <= ring.  Returns WA_EINVAL otherwise.
+ */
+int wa_prompt(const void* q, const void* k, const void* v, int32_t p0, int32_t n,
+              const int32_t* hi, int32_t hq, int32_t hkv, int32_t d, int32_t win, int32_t ring,
+              float scale, int32_t p32, const wa_strides* strides, void* out,
+              void* ws, size_t ws_bytes, void* stream);
+
+/* Waits for `stream`, then returns the WA_STATUS_* bits the last call that
+ * used `ws` left (0 when clean), or a negative WA_E* code if the read fails. */
+int wa_status(const void* ws, void* stream);
+
+/* Static description of a WA_* return code or WA_STATUS_* bit set. */
+const char* wa_strerror(int code);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int wa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WA_H */

@@ -1,0 +1,182 @@
+"""Sliding-window grouped-query attention for one GB300 (sm_103a).
+
+A thin ctypes binding of ``libwa.so`` (the C ABI declared in ``include/wa.h``):
+it checks dtypes and devices, turns tensors into pointers and strides, and
+calls the library on the current CUDA stream.  Every step of the attention
+runs in the library's CUDA kernels; there is no Python or CPU fallback, and
+calling an entry point without the built library raises.
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+__all__ = [
+    "WAError", "lib", "lib_path", "decode", "prompt", "status", "decode_ws_bytes", "prompt_ws_bytes",
+    "WA_OK", "WA_EINVAL", "WA_EWORKSPACE", "WA_ECUDA", "WA_EDEVICE",
+    "WA_STATUS_BAD_POS", "WA_STATUS_BAD_HI", "WA_STATUS_TIMEOUT",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libwa.so")
+_HEADER = os.path.join(os.path.dirname(_HERE), "include", "wa.h")
+
+
+def _header_constants() -> dict:
+    consts = {}
+    with open(_HEADER) as f:
+        for line in f:
+            m = re.match(r"#define\s+(WA_\w+)\s+\(?(-?\d+)\)?", line)
+            if m:
+                consts[m.group(1)] = int(m.group(2))
+    return consts
+
+
+_C = _header_constants()
+WA_OK = _C["WA_OK"]
+WA_EINVAL = _C["WA_EINVAL"]
+WA_EWORKSPACE = _C["WA_EWORKSPACE"]
+WA_ECUDA = _C["WA_ECUDA"]
+WA_EDEVICE = _C["WA_EDEVICE"]
+WA_STATUS_BAD_POS = _C["WA_STATUS_BAD_POS"]
+WA_STATUS_BAD_HI = _C["WA_STATUS_BAD_HI"]
+WA_STATUS_TIMEOUT = _C["WA_STATUS_TIMEOUT"]
+
+
+class WAError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {lib().wa_strerror(code).decode()} ({code})")
+
+
+class _Strides(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_int64), ("k", ctypes.c_int64), ("v", ctypes.c_int64), ("out", ctypes.c_int64)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(_LIB_PATH)
+        L.wa_decode_ws_bytes.argtypes = [_I, _I, _I, _I, _I]
+        L.wa_decode_ws_bytes.restype = ctypes.c_size_t
+        L.wa_decode.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, ctypes.c_size_t, _P]
+        L.wa_decode.restype = ctypes.c_int
+        L.wa_prompt_ws_bytes.argtypes = [_I, _I]
+        L.wa_prompt_ws_bytes.restype = ctypes.c_size_t
+        L.wa_prompt.argtypes = [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, ctypes.c_float, _I,
+                                ctypes.POINTER(_Strides), _P, _P, ctypes.c_size_t, _P]
+        L.wa_prompt.restype = ctypes.c_int
+        L.wa_status.argtypes = [_P, _P]
+        L.wa_status.restype = ctypes.c_int
+        L.wa_strerror.argtypes = [ctypes.c_int]
+        L.wa_strerror.restype = ctypes.c_char_p
+        L.wa_version.argtypes = []
+        L.wa_version.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _check_bf16(name: str, t: torch.Tensor) -> None:
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a bf16 CUDA tensor")
+
+
+def decode_ws_bytes(rows: int, hq: int, d: int, win: int, ring: int) -> int:
+    return int(lib().wa_decode_ws_bytes(rows, hq, d, win, ring))
+
+
+def prompt_ws_bytes(n: int, hq: int) -> int:
+    return int(lib().wa_prompt_ws_bytes(n, hq))
+
+
+def _workspace(nbytes: int, device, ws):
+    if ws is None:
+        return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    return ws
+
+
+def decode(q, k_ring, v_ring, pos, win: int, scale: float = 1.0, out=None, ws=None, stream=None):
+    """Decode attention: q [rows,hq,d], k_ring/v_ring [rows,ring,hkv,d] (bf16, dense), pos int32 [rows].
+
+    Returns out [rows,hq,d] bf16.  ``ws`` may be a reused uint8 CUDA buffer of
+    at least decode_ws_bytes(...) bytes; the call is asynchronous on ``stream``."""
+    for n_, t in (("q", q), ("k_ring", k_ring), ("v_ring", v_ring)):
+        _check_bf16(n_, t)
+        if not t.is_contiguous():
+            raise ValueError(f"{n_} must be contiguous")
+    if pos.dtype != torch.int32 or not pos.is_cuda:
+        raise TypeError("pos must be an int32 CUDA tensor")
+    rows, hq, d = q.shape
+    _, ring, hkv, _ = k_ring.shape
+    if out is None:
+        out = torch.empty_like(q)
+    nbytes = decode_ws_bytes(rows, hq, d, win, ring)
+    ws = _workspace(nbytes, q.device, ws)
+    rc = lib().wa_decode(q.data_ptr(), k_ring.data_ptr(), v_ring.data_ptr(), pos.data_ptr(), rows, hq, hkv, d,
+                         win, ring, float(scale), out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream))
+    if rc != WA_OK:
+        raise WAError(rc, "wa_decode")
+    return out
+
+
+def _token_stride(name: str, t: torch.Tensor, d: int) -> int:
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != d:
+        raise ValueError(f"{name} must be [tokens, heads, d] with head stride d and unit dim stride")
+    return int(t.stride(0))
+
+
+def prompt(q, k, v, p0: int, hi=None, win: int = 0, scale: float = 1.0, p32: bool = False,
+           out=None, ws=None, stream=None):
+    """Prompt attention for rows p0 .. p0+n-1: q [n,hq,d], k/v [ring,hkv,d] (bf16, token-strided).
+
+    ``hi`` is None (each row's last key is its own position) or an int32 CUDA
+    tensor [n].  Returns out [n,hq,d] bf16."""
+    for n_, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16(n_, t)
+    n, hq, d = q.shape
+    ring, hkv, _ = k.shape
+    if hi is not None and (hi.dtype != torch.int32 or not hi.is_cuda or hi.numel() != n):
+        raise TypeError("hi must be None or an int32 CUDA tensor of n elements")
+    if out is None:
+        out = torch.empty((n, hq, d), dtype=torch.bfloat16, device=q.device)
+    st = _Strides(_token_stride("q", q, d), _token_stride("k", k, d), _token_stride("v", v, d),
+                  _token_stride("out", out, d))
+    ws = _workspace(prompt_ws_bytes(n, hq), q.device, ws)
+    rc = lib().wa_prompt(q.data_ptr(), k.data_ptr(), v.data_ptr(), int(p0), n,
+                         None if hi is None else hi.data_ptr(), hq, hkv, d, int(win), ring, float(scale),
+                         1 if p32 else 0, ctypes.byref(st), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                         _stream_handle(stream))
+    if rc != WA_OK:
+        raise WAError(rc, "wa_prompt")
+    return out
+
+
+def status(ws, stream=None) -> int:
+    """WA_STATUS_* bits of the last call on ``ws`` (waits for the stream)."""
+    rc = lib().wa_status(ws.data_ptr(), _stream_handle(stream))
+    if rc < 0:
+        raise WAError(rc, "wa_status")
+    return rc

@@ -1,0 +1,73 @@
+// wa_internal.h — launch-side structures shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace wa {
+
+constexpr int kChunk = 256;     // decode: keys per chunk, at absolute positions [256c, 256c+255]
+constexpr int kHeaderBytes = 256;
+
+// First 256 bytes of every workspace.  The per-call clear resets them.
+struct WsHeader {
+    int status;   // WA_STATUS_* bits
+    int nflag;    // (row, head) pairs queued for the float64 re-run
+    int pad[62];
+};
+
+inline int decode_chunks_max(int win, int ring) {
+    return win > 0 ? (win - 1 + kChunk - 1) / kChunk + 1 : (ring + kChunk - 1) / kChunk;
+}
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* pos;
+    int rows, hq, hkv, d, win, ring;
+    float scale;
+    void* out;
+    WsHeader* hdr;
+    int* flags;      // [rows * hq]
+    float* part;     // [rows, hq, cmax, d + 4]
+    int cmax;
+};
+
+struct PromptArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* hi;   // may be null
+    int p0, n, hq, hkv, d, win, ring;
+    float scale;
+    int p32;
+    int64_t q_tok, k_tok, v_tok, o_tok;   // token strides, elements
+    void* out;
+    WsHeader* hdr;
+    int* flags;      // [n * hq]
+};
+
+// Float64 re-run of every flagged (row, head); mode 0 = decode, 1 = prompt.
+struct RerunArgs {
+    int mode;
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* idx;  // decode: pos; prompt: hi (may be null)
+    int rows, hq, hkv, d, win, ring, p0;
+    float scale;
+    int64_t q_tok, k_tok, v_tok, o_tok;   // prompt token strides; decode uses dense layouts
+    void* out;
+    WsHeader* hdr;
+    const int* flags;
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_prompt(const PromptArgs& a, cudaStream_t s);
+cudaError_t launch_rerun(const RerunArgs& a, cudaStream_t s);
+cudaError_t prompt_prepare_device(int dev);
+cudaError_t decode_prepare_device(int dev);
+
+}  // namespace wa
