@@ -43,7 +43,8 @@ struct PartCfg {
     static constexpr int MW_OFF = SC_OFF + kChunk * G * 4;      // run maxima [8][G]
     static constexpr int LW_OFF = MW_OFF + kRuns * G * 4;       // run sums [8][G]
     static constexpr int BAR_OFF = (LW_OFF + kRuns * G * 4 + 15) & ~15;
-    static constexpr int SMEM = BAR_OFF + 2 * STAGES * 8;
+    static constexpr int NLOADS = 2 * kRuns;                    // K runs, then V runs
+    static constexpr int SMEM = BAR_OFF + 2 * NLOADS * 8;        // full[t], consumed[t]
     static constexpr int MIN_BLOCKS = (G <= 4) ? 2 : 1;
 };
 
@@ -119,13 +120,17 @@ decode_part_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     float* sc = reinterpret_cast<float*>(smem + C::SC_OFF);
     float* mw = reinterpret_cast<float*>(smem + C::MW_OFF);
     float* lw = reinterpret_cast<float*>(smem + C::LW_OFF);
+    // Load t (K run w0+t for t < nr, then V run w0+t-nr) lands in stage t % STAGES.
+    // Each load has its own single-use barriers: full[t] (bytes landed) and
+    // consumed[t] (stage free again), so every wait is on phase 0 of a fresh
+    // barrier and no waiter can confuse one use of a stage with another.
     const uint32_t bar_full = smem_u32(smem + C::BAR_OFF);
-    const uint32_t bar_empty = bar_full + 8 * C::STAGES;
+    const uint32_t bar_used = bar_full + 8 * C::NLOADS;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+        for (int t = 0; t < C::NLOADS; ++t) {
+            mbar_init(bar_full + 8 * t, 1);
+            mbar_init(bar_used + 8 * t, 1);
         }
         fence_mbar_init();
     }
@@ -139,25 +144,24 @@ decode_part_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
         int issued = 0;
         bool ok = true;
         for (int t = 0; t < 2 * nr; ++t) {
-            const int st = t % C::STAGES, u = t / C::STAGES;
-            if (u > 0 && !mbar_wait(bar_empty + 8 * st, (u - 1) & 1, status)) { ok = false; break; }
+            const int st = t % C::STAGES;
+            if (t >= C::STAGES && !mbar_wait(bar_used + 8 * (t - C::STAGES), 0, status)) { ok = false; break; }
             const int run = w0 + (t % nr);
             const __nv_bfloat16* src_base = (t < nr) ? k : v;
             const int rb = cbase + run * kRun;
             const int a = max(kb, rb), b = min(ke, rb + kRun - 1);
             const int j = rb + lane;
-            if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * st, static_cast<uint32_t>((b - a + 1) * C::ROWB));
+            if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * t, static_cast<uint32_t>((b - a + 1) * C::ROWB));
             __syncwarp();
             if (j >= a && j <= b) {
                 const __nv_bfloat16* src = src_base + ((row0 + static_cast<size_t>(j % ring)) * hkv + g) * D;
-                bulk_g2s(smem_u32(stage + st * C::STAGE_B + lane * C::ROWB), src, C::ROWB, bar_full + 8 * st, pol);
+                bulk_g2s(smem_u32(stage + st * C::STAGE_B + lane * C::ROWB), src, C::ROWB, bar_full + 8 * t, pol);
             }
             issued = t + 1;
         }
         if (!ok && lane == 0) {
             // a consumer stopped: let the copies already issued land before the CTA can exit
-            for (int t = max(0, issued - C::STAGES); t < issued; ++t)
-                mbar_wait(bar_full + 8 * (t % C::STAGES), (t / C::STAGES) & 1, status);
+            for (int t = max(0, issued - C::STAGES); t < issued; ++t) mbar_wait(bar_full + 8 * t, 0, status);
         }
         return;
     }
@@ -190,7 +194,7 @@ decode_part_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     if (active) {
         const int t = w - w0;
         const int st = t % C::STAGES;
-        ok = mbar_wait(bar_full + 8 * st, (t / C::STAGES) & 1, status);
+        ok = mbar_wait(bar_full + 8 * t, 0, status);
         if (ok) {
             const uint8_t* base = stage + st * C::STAGE_B;
             for (int jj = a - rb; jj <= b - rb; ++jj) {
@@ -211,7 +215,7 @@ decode_part_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+            if (lane == 0) mbar_arrive(bar_used + 8 * t);
         }
     }
     if (lane == 0) {
@@ -249,7 +253,7 @@ decode_part_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
         __syncwarp();
         const int t = nr + (w - w0);
         const int st = t % C::STAGES;
-        ok = mbar_wait(bar_full + 8 * st, (t / C::STAGES) & 1, status);
+        ok = mbar_wait(bar_full + 8 * t, 0, status);
         if (ok) {
             const uint8_t* base = stage + st * C::STAGE_B;
             for (int jj = a - rb; jj <= b - rb; ++jj) {
@@ -264,7 +268,7 @@ decode_part_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+            if (lane == 0) mbar_arrive(bar_used + 8 * t);
         }
     }
     if (lane == 0) {
