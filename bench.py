@@ -1,0 +1,664 @@
+#!/usr/bin/env python3
+"""Throughput of the sliding-window GQA hot path on GB300, as a fraction of the roofline.
+
+One step runs the whole path once over a fixed synthetic workload, shaped like
+the pages' workloads (TensorFold pull request #1123, "Receipt"; the "Exact
+Numerical Contract" page, "Canonical Boundary"):
+
+  decode_sliding  3 independent caches x 64 rows, 32/16 heads, d 256, window 1024
+                  over a ring of 1536, positions uniform to 40,000, three streams
+  decode_linear   64 rows, 32/16 heads, d 256, linear cache of 32,768 keys
+  prompt_causal   8,192 rows at p0 0, 16/8 heads, d 256, linear cache, causal, P32
+  prompt_dense    37,810 rows, 56 heads (MHA), d 128, interleaved QKV (row 21,504),
+                  RMSNormed Q/K, scale 1/sqrt(128), non-causal (hi = N-1), bf16 P
+
+value = (decode bytes / HBM peak + prompt flops / bf16 peak) / measured step time:
+the step's roofline time over its measured time.  Decode bytes are the visible
+K and V rows plus q and out; prompt flops are 4*d per visible (row, key, head).
+Peaks come from MEASURED_PEAKS.json (the sustained bf16 figure, since each
+kernel runs inside a long step).
+
+Prints one JSON line.  --impl reference times the float64 oracle on the host
+cores on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode KV-read GB/s and prompt attention TFLOP/s, as fraction of GB300 roofline"
+UNIT = "fraction of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+PARTS = ("decode_sliding", "decode_linear", "prompt_causal", "prompt_dense")
+SPEC = {
+    "decode_sliding": dict(caches=3, rows=64, hq=32, hkv=16, d=256, win=1024, ring=1536, pos_max=40000,
+                           seed=20260003),
+    "decode_linear": dict(rows=64, hq=32, hkv=16, d=256, win=0, ring=32768, seed=20260004),
+    "prompt_causal": dict(n=8192, p0=0, hq=16, hkv=8, d=256, win=0, ring=8192, p32=True, seed=20260005),
+    "prompt_dense": dict(N=37810, H=56, d=128, p32=False, seed=20260006),
+}
+
+# ncu DRAM bytes per launch of the dominant kernels, valid only while the kernel source is unchanged.
+TRAFFIC = {}
+
+
+# ----------------------------------------------------------------------------- work accounting
+
+def decode_positions(part: str):
+    import torch
+    s = SPEC[part]
+    g = torch.Generator().manual_seed(s["seed"])
+    if part == "decode_sliding":
+        out = []
+        for _ in range(s["caches"]):
+            p = torch.randint(0, s["pos_max"] + 1, (s["rows"],), generator=g).tolist()
+            p[0] = s["pos_max"]
+            out.append(p)
+        return out
+    p = torch.randint(0, s["ring"], (s["rows"],), generator=g).tolist()
+    p[5] = s["ring"] - 1
+    return [p]
+
+
+def visible(p: int, win: int) -> int:
+    lo = max(0, p - win + 1) if win > 0 else 0
+    return p - lo + 1
+
+
+def decode_bytes(pos, hq, hkv, d, win) -> int:
+    """K and V rows each row reads (hkv * visible * d * 2 bytes, twice) plus q and out."""
+    kv = sum(hkv * visible(p, win) * d * 2 * 2 for p in pos)
+    return kv + 2 * len(pos) * hq * d * 2
+
+
+def prompt_flops_rows(rows, p0, win, hi_of, hq, d) -> int:
+    """4*d flops (2d for q.k, 2d for p.v) per visible (row, key, head)."""
+    tot = 0
+    for i in rows:
+        p = p0 + i
+        lo = max(0, p - win + 1) if win > 0 else 0
+        tot += hi_of(i) - lo + 1
+    return tot * hq * 4 * d
+
+
+def part_work(part: str):
+    s = SPEC[part]
+    if part.startswith("decode"):
+        return {"bytes": sum(decode_bytes(p, s["hq"], s["hkv"], s["d"], s["win"]) for p in decode_positions(part)),
+                "flops": 0}
+    if part == "prompt_causal":
+        n = s["n"]
+        vis = n * (n + 1) // 2          # row i sees keys 0..i
+        return {"bytes": 0, "flops": vis * s["hq"] * 4 * s["d"], "issued_flops_factor": 1.5 if s["p32"] else 1.0}
+    N = s["N"]
+    return {"bytes": 0, "flops": N * N * s["H"] * 4 * s["d"], "issued_flops_factor": 1.5 if s["p32"] else 1.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])), "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def roofline_seconds(parts, pk) -> float:
+    t = 0.0
+    for part in parts:
+        w = part_work(part)
+        t += w["bytes"] / (pk["hbm_gbs"] * 1e9) + w["flops"] / (pk["bf16_tflops_sustained"] * 1e12)
+    return t
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- native arm
+
+class Part:
+    name = ""
+    launches = 0
+
+    def run(self, stream):
+        raise NotImplementedError
+
+
+def _events(torch, stream, n=2):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+class DecodeSliding(Part):
+    name = "decode_sliding"
+
+    def __init__(self, torch, wa, wa_synth, dev):
+        s = SPEC[self.name]
+        self.torch, self.wa = torch, wa
+        self.cases, self.outs, self.ws = [], [], []
+        for i, pos in enumerate(decode_positions(self.name)):
+            c = wa_synth.decode_case(s["rows"], s["hq"], s["hkv"], s["d"], s["win"], s["ring"], pos,
+                                     seed=s["seed"] * 10 + i, device=dev, outside="keep")
+            self.cases.append(c)
+            self.outs.append(torch.empty_like(c["q"]))
+            self.ws.append(torch.empty(wa.decode_ws_bytes(s["rows"], s["hq"], s["d"], s["win"], s["ring"]),
+                                       dtype=torch.uint8, device=dev))
+        self.streams = [torch.cuda.Stream(device=dev) for _ in self.cases]
+        self.launches = 3 * len(self.cases)   # partial, merge, float64 re-run per cache
+        self.start_ev = torch.cuda.Event(enable_timing=True)
+        self.join_ev = torch.cuda.Event(enable_timing=True)
+        self.end_evs = [torch.cuda.Event() for _ in self.cases]
+        self.kernel_ms = []
+
+    def run(self, stream, host=None):
+        torch, wa, s = self.torch, self.wa, SPEC[self.name]
+        self.start_ev.record(stream)
+        for i, (c, st) in enumerate(zip(self.cases, self.streams)):
+            st.wait_event(self.start_ev)
+            with torch.cuda.stream(st):
+                if host is not None:
+                    for key in ("q", "k", "v", "pos"):
+                        c[key].copy_(host[i][key], non_blocking=True)
+                wa.decode(c["q"], c["k"], c["v"], c["pos"], s["win"], 1.0, out=self.outs[i], ws=self.ws[i], stream=st)
+                if host is not None:
+                    host[i]["out"].copy_(self.outs[i], non_blocking=True)
+            self.end_evs[i].record(st)
+            stream.wait_event(self.end_evs[i])
+        self.join_ev.record(stream)
+
+    def collect(self):
+        # wall time of the three concurrent calls, from the fork to the join on the main stream
+        self.kernel_ms.append(self.start_ev.elapsed_time(self.join_ev))
+
+    def host_buffers(self):
+        hb = []
+        for c, o in zip(self.cases, self.outs):
+            d = {k: c[k].cpu().pin_memory() for k in ("q", "k", "v", "pos")}
+            d["out"] = torch_empty_pinned_like(o)
+            hb.append(d)
+        return hb
+
+
+def torch_empty_pinned_like(t):
+    import torch
+    return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+
+
+class DecodeLinear(Part):
+    name = "decode_linear"
+
+    def __init__(self, torch, wa, wa_synth, dev):
+        s = SPEC[self.name]
+        self.torch, self.wa = torch, wa
+        pos = decode_positions(self.name)[0]
+        self.c = wa_synth.decode_case(s["rows"], s["hq"], s["hkv"], s["d"], s["win"], s["ring"], pos,
+                                      seed=s["seed"], device=dev, outside="keep")
+        self.out = torch.empty_like(self.c["q"])
+        self.ws = torch.empty(wa.decode_ws_bytes(s["rows"], s["hq"], s["d"], s["win"], s["ring"]),
+                              dtype=torch.uint8, device=dev)
+        self.launches = 3
+        self.k_start, self.k_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.kernel_ms = []
+
+    def run(self, stream, host=None):
+        s, c = SPEC[self.name], self.c
+        if host is not None:
+            for key in ("q", "k", "v", "pos"):
+                c[key].copy_(host[key], non_blocking=True)
+        self.k_start.record(stream)
+        self.wa.decode(c["q"], c["k"], c["v"], c["pos"], s["win"], 1.0, out=self.out, ws=self.ws, stream=stream)
+        self.k_end.record(stream)
+        if host is not None:
+            host["out"].copy_(self.out, non_blocking=True)
+
+    def collect(self):
+        self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
+
+    def host_buffers(self):
+        d = {k: self.c[k].cpu().pin_memory() for k in ("q", "k", "v", "pos")}
+        d["out"] = torch_empty_pinned_like(self.out)
+        return d
+
+
+class PromptCausal(Part):
+    name = "prompt_causal"
+
+    def __init__(self, torch, wa, wa_synth, dev):
+        s = SPEC[self.name]
+        self.torch, self.wa = torch, wa
+        self.c = wa_synth.prompt_case(s["n"], s["p0"], s["hq"], s["hkv"], s["d"], s["win"], s["ring"],
+                                      seed=s["seed"], device=dev, outside="keep")
+        self.out = torch.empty_like(self.c["q"])
+        self.ws = torch.empty(wa.prompt_ws_bytes(s["n"], s["hq"]), dtype=torch.uint8, device=dev)
+        self.launches = 2   # prompt kernel, float64 re-run
+        self.k_start, self.k_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.kernel_ms = []
+
+    def run(self, stream, host=None):
+        s, c = SPEC[self.name], self.c
+        if host is not None:
+            for key in ("q", "k", "v"):
+                c[key].copy_(host[key], non_blocking=True)
+        self.k_start.record(stream)
+        self.wa.prompt(c["q"], c["k"], c["v"], s["p0"], None, s["win"], 1.0, p32=s["p32"], out=self.out, ws=self.ws,
+                       stream=stream)
+        self.k_end.record(stream)
+        if host is not None:
+            host["out"].copy_(self.out, non_blocking=True)
+
+    def collect(self):
+        self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
+
+    def host_buffers(self):
+        d = {k: self.c[k].cpu().pin_memory() for k in ("q", "k", "v")}
+        d["out"] = torch_empty_pinned_like(self.out)
+        return d
+
+
+class PromptDense(Part):
+    name = "prompt_dense"
+
+    def __init__(self, torch, wa, wa_synth, dev):
+        s = SPEC[self.name]
+        self.torch, self.wa = torch, wa
+        self.c = wa_synth.dense_qkv_case(s["N"], s["H"], s["d"], seed=s["seed"], device=dev)
+        self.hi = torch.full((s["N"],), s["N"] - 1, dtype=torch.int32, device=dev)
+        self.out = torch.empty((s["N"], s["H"], s["d"]), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(wa.prompt_ws_bytes(s["N"], s["H"]), dtype=torch.uint8, device=dev)
+        self.launches = 2
+        self.k_start, self.k_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.kernel_ms = []
+
+    def run(self, stream, host=None):
+        s, c = SPEC[self.name], self.c
+        if host is not None:
+            c["qkv"].copy_(host["qkv"], non_blocking=True)
+            self.hi.copy_(host["hi"], non_blocking=True)
+        self.k_start.record(stream)
+        self.wa.prompt(c["q"], c["k"], c["v"], 0, self.hi, 0, c["scale"], p32=s["p32"], out=self.out, ws=self.ws,
+                       stream=stream)
+        self.k_end.record(stream)
+        if host is not None:
+            host["out"].copy_(self.out, non_blocking=True)
+
+    def collect(self):
+        self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
+
+    def host_buffers(self):
+        return {"qkv": self.c["qkv"].cpu().pin_memory(), "hi": self.hi.cpu().pin_memory(),
+                "out": torch_empty_pinned_like(self.out)}
+
+
+PART_CLASSES = {"decode_sliding": DecodeSliding, "decode_linear": DecodeLinear,
+                "prompt_causal": PromptCausal, "prompt_dense": PromptDense}
+
+KERNEL_OF = {"decode_sliding": "decode partial (wa_decode.cu)", "decode_linear": "decode partial (wa_decode.cu)",
+             "prompt_causal": "prompt tensor-core tile (wa_prompt.cu)",
+             "prompt_dense": "prompt tensor-core tile (wa_prompt.cu)"}
+SOURCE_OF = {"decode_sliding": "wa_decode.cu", "decode_linear": "wa_decode.cu",
+             "prompt_causal": "wa_prompt.cu", "prompt_dense": "wa_prompt.cu"}
+
+
+def source_hash(fname: str) -> str:
+    p = os.path.join(ROOT, "sliding_window_gqa_gb300", "csrc", fname)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def io_bytes(obj) -> int:
+    import torch
+    if isinstance(obj, torch.Tensor):
+        return obj.numel() * obj.element_size()
+    if isinstance(obj, dict):
+        return sum(io_bytes(v) for v in obj.values())
+    if isinstance(obj, (list, tuple)):
+        return sum(io_bytes(v) for v in obj)
+    return 0
+
+
+def run_native(args, parts, rank, world, dist):
+    import torch
+
+    import sliding_window_gqa_gb300 as wa
+    import wa_synth
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wa.lib()
+    objs = [PART_CLASSES[p](torch, wa, wa_synth, dev) for p in parts]
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step(host=None):
+        for i, o in enumerate(objs):
+            o.run(stream, None if host is None else host[i])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for o in objs:
+        o.kernel_ms = []
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step()
+        torch.cuda.synchronize()      # per-step event reads; the region stays GPU-timed end to end
+        for o in objs:
+            o.collect()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    # e2e: the same step through the C ABI with host buffers (H2D of inputs, D2H of outputs each step)
+    e2e = None
+    if not args.no_e2e:
+        host = [o.host_buffers() for o in objs]
+        torch.cuda.synchronize()
+        step(host)
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ksteps = max(1, min(args.steps, args.e2e_steps))
+        e0.record(stream)
+        for _ in range(ksteps):
+            step(host)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / ksteps
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = sum(io_bytes({k: v for k, v in h.items() if k != "out"}) if isinstance(h, dict)
+                  else sum(io_bytes({k: v for k, v in x.items() if k != "out"}) for x in h) for h in host)
+        d2h = sum(io_bytes(h["out"]) if isinstance(h, dict) else sum(io_bytes(x["out"]) for x in h) for h in host)
+        e2e = {"ms_per_step": e_ms, "steps": ksteps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        del host
+    per_part_ms = {o.name: statistics.median(o.kernel_ms) for o in objs}
+    launches = sum(o.launches for o in objs) * args.steps
+    return ms_per_step, per_part_ms, clk, e2e, launches
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arm
+
+def oracle_sample(parts, budget_s: float):
+    """Times the float64 oracle on a bounded sample of each part and extrapolates to the full part.
+
+    Returns (seconds for the full workload, description, threads)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import wa_synth
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    per = budget_s / max(1, len(parts))
+    total, desc = 0.0, []
+    for part in parts:
+        s = SPEC[part]
+        w = part_work(part)
+        if part.startswith("decode"):
+            pos_all = [p for ps in decode_positions(part) for p in ps]
+            rows_done, work_done, t_used, i = 0, 0, 0.0, 0
+            while t_used < per and i < len(pos_all):
+                p = pos_all[i]
+                c = wa_synth.decode_case(1, s["hq"], s["hkv"], s["d"], s["win"], s["ring"], [p],
+                                         seed=s["seed"] + i, outside="keep", peaked=False)
+                t0 = time.perf_counter()
+                oracle.decode(bits(c["q"]), bits(c["k"]), bits(c["v"]), [p], s["win"], s["ring"], 1.0)
+                t_used += time.perf_counter() - t0
+                work_done += decode_bytes([p], s["hq"], s["hkv"], s["d"], s["win"])
+                rows_done += 1
+                i += 1
+            total += t_used * w["bytes"] / work_done
+            desc.append(f"{part}: {rows_done} rows of {len(pos_all)}")
+        elif part == "prompt_causal":
+            n = s["n"]
+            c = wa_synth.prompt_case(n, s["p0"], s["hq"], s["hkv"], s["d"], s["win"], s["ring"], seed=s["seed"],
+                                     outside="keep", peaked=False)
+            q, k, v = bits(c["q"]), bits(c["k"]), bits(c["v"])
+            rng = np.random.default_rng(s["seed"])
+            rows_done, t_used, flops_done = 0, 0.0, 0
+            while t_used < per and rows_done < 64:
+                i = int(rng.integers(0, n))
+                t0 = time.perf_counter()
+                oracle.prompt(q, k, v, s["p0"], s["win"], s["ring"], 1.0, rows=[i])
+                t_used += time.perf_counter() - t0
+                flops_done += prompt_flops_rows([i], s["p0"], s["win"], lambda r: s["p0"] + r, s["hq"], s["d"])
+                rows_done += 1
+            total += t_used * w["flops"] / flops_done
+            desc.append(f"{part}: {rows_done} random rows of {n}, all heads")
+        else:
+            N, H, d = s["N"], 2, s["d"]            # two heads of the 56: per-head work is identical
+            c = wa_synth.dense_qkv_case(N, H, d, seed=s["seed"])
+            q, k, v = bits(c["q"]), bits(c["k"]), bits(c["v"])
+            rows = list(range(0, N, max(1, N // 64)))[:64]
+            t0 = time.perf_counter()
+            oracle.prompt(q, k, v, 0, 0, N, c["scale"], hi=np.full(N, N - 1), rows=rows)
+            t_used = time.perf_counter() - t0
+            flops_done = len(rows) * N * H * 4 * d
+            total += t_used * w["flops"] / flops_done
+            desc.append(f"{part}: {len(rows)} rows x {H} heads of {N} x {s['H']}")
+    return total, "; ".join(desc)
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, parts):
+    pk = peaks()
+    t_roof = roofline_seconds(parts, pk)
+    times = []
+    budget = args.ref_budget
+    for _ in range(args.warmup):
+        oracle_sample(parts, budget / 4)
+    desc = ""
+    for _ in range(args.steps):
+        t, desc = oracle_sample(parts, budget)
+        times.append(t)
+    t_step = statistics.median(times)
+    value = t_roof / t_step
+    cores = cpu_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(parts),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc + " (per step; extrapolated to the full workload by work)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(parts):
+    return {"workload": " + ".join(parts), "parts": {p: SPEC[p] for p in parts},
+            "l2": "inputs larger than L2 (each step streams > 40 GB of K/V and QKV); no flush",
+            "peaks": "MEASURED_PEAKS.json hbm_gbs and bf16_tflops_sustained"}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--parts", default="all", help="comma list of " + ",".join(PARTS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=8.0, help="oracle seconds per reference step")
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="oracle seconds for cpu_baseline")
+    ap.add_argument("--caches", type=int, default=None, help="override the decode_sliding cache count (profiling)")
+    args = ap.parse_args()
+    if args.caches is not None:
+        SPEC["decode_sliding"]["caches"] = args.caches
+    args.warmup = max(args.warmup, 3)
+    parts = list(PARTS) if args.parts == "all" else [p for p in args.parts.split(",") if p]
+    for p in parts:
+        if p not in PARTS:
+            raise SystemExit(f"unknown part {p}")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, parts)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    ms_per_step, per_part_ms, clk, e2e, launches = run_native(args, parts, rank, world, dist)
+    pk = peaks()
+    t_roof = roofline_seconds(parts, pk)
+    value_one = t_roof / (ms_per_step * 1e-3)
+    value = value_one * world            # every rank runs its own copy of the workload (weak scaling)
+
+    part_report = {}
+    for p in parts:
+        w = part_work(p)
+        ms = per_part_ms[p]
+        if w["bytes"]:
+            gbs = w["bytes"] / (ms * 1e-3) / 1e9
+            part_report[p] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "bytes": w["bytes"]}
+        else:
+            tf = w["flops"] / (ms * 1e-3) / 1e12
+            part_report[p] = {"ms": ms, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops_sustained"],
+                              "flops": w["flops"], "issued_TFLOP/s": tf * w.get("issued_flops_factor", 1.0)}
+    dom = max(parts, key=lambda p: per_part_ms[p])
+    w = part_work(dom)
+    ms = per_part_ms[dom]
+    if w["bytes"]:
+        ach = w["bytes"] / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"]}
+    else:
+        ach = w["flops"] / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_tflops_sustained"]}
+    tr = TRAFFIC.get(dom)
+    roof["traffic"] = tr["bytes_per_launch"] if tr and tr.get("source_sha") == source_hash(SOURCE_OF[dom]) else None
+    roof["kernel"] = KERNEL_OF[dom] + f", part {dom}; per-launch time from CUDA events around the C-ABI call"
+    roof["peak_source"] = pk["source"] + (" (sustained bf16)" if roof["bound"] == "tensor" else " (copy GB/s)")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_block(parts),
+        "parts": part_report, "roofline": roof, "clocks": clk, "gpu_launches": launches,
+    }
+    if e2e is not None:
+        line["e2e"] = {"value": t_roof * world / (e2e["ms_per_step"] * 1e-3), "unit": UNIT,
+                       "h2d_bytes_per_step": e2e["h2d_bytes_per_step"], "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                       "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"]}
+    if rank == 0 and not args.no_cpu_baseline:
+        t_cpu, desc = oracle_sample(parts, args.cpu_budget)
+        line["cpu_baseline"] = {"value": t_roof / t_cpu, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                                "sample": desc + "; extrapolated to the full workload by work"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
