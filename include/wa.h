@@ -44,6 +44,10 @@ extern "C" {
 #define WA_EWORKSPACE (-2)    /* ws is null, misaligned or smaller than the *_ws_bytes query */
 #define WA_ECUDA (-3)         /* a CUDA call or launch failed */
 #define WA_EDEVICE (-4)       /* the current device is not a compute capability 10.3 GPU */
+#define WA_ESTATIC (-5)       /* wa_decode_static: these sizes need more than WA_STATIC_WS_BYTES of scratch */
+
+/* Size of the library-owned scratch array behind wa_decode_static (16 MiB per device). */
+#define WA_STATIC_WS_BYTES (16u * 1024u * 1024u)
 
 #define WA_STATUS_BAD_POS 1   /* a decode pos was < 0, or >= ring with win = 0 (clamped) */
 #define WA_STATUS_BAD_HI 2    /* a prompt hi[i] was outside [p0+i, p0+n-1] (clamped) */
@@ -83,6 +87,31 @@ size_t wa_decode_ws_bytes(int32_t rows, int32_t hq, int32_t d, int32_t win, int3
 int wa_decode(const void* q, const void* k_ring, const void* v_ring, const int32_t* pos,
               int32_t rows, int32_t hq, int32_t hkv, int32_t d, int32_t win, int32_t ring,
               float scale, void* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * wa_decode_static — wa_decode without a caller workspace.  The pages have no
+ * counterpart; it exists for callers that cannot allocate device memory: a
+ * plug-in inside a host framework that owns all device memory and gives
+ * plug-ins no allocator, or a serving loop that forbids cudaMalloc after
+ * start-up because it can synchronize the device and stall every stream.
+ *
+ * Arguments, layouts and results are those of wa_decode.  The scratch (chunk
+ * partials, status word, re-run list) is one library-owned device array of
+ * WA_STATIC_WS_BYTES per device, held from library load until process exit;
+ * sizes whose wa_decode_ws_bytes exceeds it return WA_ESTATIC before anything
+ * is enqueued.  Nothing is allocated or freed.
+ *
+ * The first call on each device looks up the array's device address (once,
+ * with that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array, and each call clears the
+ * status word and re-run counter at its start: calls whose work can overlap
+ * on the GPU (for example, calls on two streams with no ordering between
+ * them) race on it and must be ordered by the caller; calls on one stream are
+ * ordered already.  The status word is not readable through wa_status.
+ */
+int wa_decode_static(const void* q, const void* k_ring, const void* v_ring, const int32_t* pos,
+                     int32_t rows, int32_t hq, int32_t hkv, int32_t d, int32_t win, int32_t ring,
+                     float scale, void* out, void* stream);
 
 /* Workspace bytes wa_prompt needs: the 256-byte header and one int32 re-run
  * slot per (row, head).  0 for invalid sizes. */

@@ -176,6 +176,7 @@ const char* wa_strerror(int code) {
         case WA_EWORKSPACE: return "workspace missing, misaligned or too small";
         case WA_ECUDA: return "CUDA call or launch failed";
         case WA_EDEVICE: return "device is not compute capability 10.3 (GB300)";
+        case WA_ESTATIC: return "sizes need more scratch than wa_decode_static's fixed 16 MiB array";
         case WA_STATUS_BAD_POS: return "status: a decode position was out of range (clamped)";
         case WA_STATUS_BAD_HI: return "status: a prompt hi[i] was out of range (clamped)";
         case WA_STATUS_TIMEOUT: return "status: a device wait ran out; outputs are not valid";
