@@ -52,7 +52,10 @@ SPEC = {
 }
 
 # ncu DRAM bytes per launch of the dominant kernels, valid only while the kernel source is unchanged.
-TRAFFIC = {}
+TRAFFIC = {
+    "prompt_dense": {"bytes_per_launch": 2068 * 10**6, "source_sha": "90bab174d9651786",
+                     "note": "ncu at N=8192 (352.5 MB read + 95.5 MB write), scaled by N to 37,810"},
+}
 
 
 # ----------------------------------------------------------------------------- work accounting
@@ -585,9 +588,12 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=8.0, help="oracle seconds per reference step")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="oracle seconds for cpu_baseline")
     ap.add_argument("--caches", type=int, default=None, help="override the decode_sliding cache count (profiling)")
+    ap.add_argument("--dense-n", type=int, default=None, help="override the prompt_dense row count (profiling)")
     args = ap.parse_args()
     if args.caches is not None:
         SPEC["decode_sliding"]["caches"] = args.caches
+    if args.dense_n is not None:
+        SPEC["prompt_dense"]["N"] = args.dense_n
     args.warmup = max(args.warmup, 3)
     parts = list(PARTS) if args.parts == "all" else [p for p in args.parts.split(",") if p]
     for p in parts:
