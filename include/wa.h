@@ -52,6 +52,7 @@ extern "C" {
 #define WA_STATUS_BAD_POS 1   /* a decode pos was < 0, or >= ring with win = 0 (clamped) */
 #define WA_STATUS_BAD_HI 2    /* a prompt hi[i] was outside [p0+i, p0+n-1] (clamped) */
 #define WA_STATUS_TIMEOUT 4   /* a bounded device wait gave up; outputs are not valid */
+#define WA_STATUS_LAYOUT 8    /* a kernel found its shared memory misaligned and wrote nothing */
 
 /* Token strides in elements for the prompt form (head stride is always d).
  * Zero means dense: hq*d for q and out, hkv*d for k and v. */

@@ -180,6 +180,7 @@ const char* wa_strerror(int code) {
         case WA_STATUS_BAD_POS: return "status: a decode position was out of range (clamped)";
         case WA_STATUS_BAD_HI: return "status: a prompt hi[i] was out of range (clamped)";
         case WA_STATUS_TIMEOUT: return "status: a device wait ran out; outputs are not valid";
+        case WA_STATUS_LAYOUT: return "status: shared memory misaligned; outputs were not written";
         default:
             if (code > 0) return "status: several WA_STATUS bits";
             return "unknown code";

@@ -34,7 +34,8 @@ namespace wa {
 namespace {
 
 constexpr int kBM = 128;           // query rows per CTA (= tensor-memory lanes)
-constexpr int kThreads = 256;      // warps 0..3 control, 4..7 softmax
+constexpr int kThreads = 384;      // warps 0..3 control, 4..7 and 8..11 softmax (two column halves)
+constexpr int kSoftmax = 256;      // softmax threads
 constexpr float kLazy = 8.0f;      // log2 units the running max may trail before O is rescaled
 
 struct PromptParams {
@@ -48,12 +49,14 @@ struct PromptParams {
     int* flags;
     int64_t k_tok, v_tok, o_tok;
     int p0, n, hq, hkv, win, ring, nqt;
-    float scale_log2;
+    float c;          // |scale| * log2(e)
+    int neg;          // scale < 0: the S MMA negates Q
 };
 
 template <int D, bool P32>
 struct Cfg {
     static constexpr int T = (D == 256) ? 64 : 128;   // keys per tile
+    static constexpr int NC = T / 2;                  // S columns per softmax thread
     static constexpr int KB = D / 64;                 // 64-element (128-byte) column blocks
     static constexpr int Q_BLOCK = kBM * 128;
     static constexpr int Q_BYTES = KB * Q_BLOCK;
@@ -66,10 +69,11 @@ struct Cfg {
     static constexpr int OFF_K = OFF_Q + Q_BYTES;               // 2 stages
     static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;          // 2 stages
     static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;          // hi, then lo for P32
-    static constexpr int OFF_BAR = OFF_P + (P32 ? 2 : 1) * P_BYTES;
-    static constexpr int NBAR = 18;
+    static constexpr int OFF_X = OFF_P + (P32 ? 2 : 1) * P_BYTES;   // row exchange [2 tiles][2 halves][128] fp32
+    static constexpr int OFF_BAR = OFF_X + 2 * 2 * kBM * 4;
+    static constexpr int NBAR = 22;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, union bounds
-    static constexpr int SMEM = OFF_MISC + 64 + 1024;           // + alignment slack
+    static constexpr int SMEM = OFF_MISC + 64;
     static constexpr int TMEM_COLS = 512;
     static constexpr int O_COL = 0;
     static constexpr int S_COL = D;                             // S buffers at D and D + T
@@ -80,7 +84,7 @@ struct Cfg {
 // barrier indices
 enum : int {
     B_Q = 0, B_KFULL = 1, B_VFULL = 3, B_VREADY = 5, B_KFREE = 7, B_VFREE = 9, B_SFULL = 11, B_SFREE = 13,
-    B_PFULL = 15, B_PVDONE = 16, B_DRAIN = 17
+    B_PFULL = 15, B_PVDONE = 16, B_DRAIN = 17, B_XCHG = 18, B_EPI_L = 20, B_EPI_B = 21
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -123,16 +127,37 @@ __device__ void copy_tile_wrapped(uint32_t dst, const uint16_t* base, int64_t to
     fence_proxy_async_smem();
 }
 
+// The NC S values of this thread's half row: raw fp32 bits from tensor memory.
+template <int NC>
+__device__ __forceinline__ void load_s(uint32_t taddr, float (&sv)[NC]) {
+    if constexpr (NC == 64) {
+        uint32_t raw[64];
+        tmem_ld64_wait(taddr, raw);
+#pragma unroll
+        for (int e = 0; e < 64; ++e) sv[e] = __uint_as_float(raw[e]);
+    } else {
+        uint32_t raw[32];
+        tmem_ld32_wait(taddr, raw);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sv[e] = __uint_as_float(raw[e]);
+    }
+}
+
 template <int D, bool P32>
 __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_constant__ PromptParams p) {
     using C = Cfg<D, P32>;
     constexpr int T = C::T;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int NC = C::NC;
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
+    if (sbase & 1023u) {   // the swizzled tiles need a 1024-byte aligned base
+        if (threadIdx.x == 0) atomicOr(p.status, WA_STATUS_LAYOUT);
+        return;
+    }
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);   // [0] tmem base, [1..4] lo min, [5..8] hi max
+    float* xbuf = reinterpret_cast<float*>(smem + C::OFF_X);            // [2][2][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = p.nqt - 1 - static_cast<int>(blockIdx.x);            // longest (causal) tiles first
@@ -150,11 +175,14 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             mbar_init(BAR(B_KFREE + s), 1);
             mbar_init(BAR(B_VFREE + s), 1);
             mbar_init(BAR(B_SFULL + s), 1);
-            mbar_init(BAR(B_SFREE + s), 4);
+            mbar_init(BAR(B_SFREE + s), 8);
+            mbar_init(BAR(B_XCHG + s), kSoftmax);
         }
-        mbar_init(BAR(B_PFULL), 4);
+        mbar_init(BAR(B_PFULL), 8);
         mbar_init(BAR(B_PVDONE), 1);
         mbar_init(BAR(B_DRAIN), 1);
+        mbar_init(BAR(B_EPI_L), kSoftmax);
+        mbar_init(BAR(B_EPI_B), kSoftmax);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -162,11 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
         tmem_relinquish();
     }
 
-    // Row ranges (softmax warps): row i sees [lo_i, hi_i]; rows past n see nothing.
+    // Row ranges (softmax warps; both halves of a row compute the same): row i sees [lo_i, hi_i].
     int row_lo = 1, row_hi = 0;
+    const int r = (warp & 3) * 32 + lane;         // the row (tensor-memory lane) of a softmax thread
+    const int i = m0 + r;
     if (warp >= 4) {
-        const int r = threadIdx.x - 128;
-        const int i = m0 + r;
         if (i < p.n) {
             const int P = p.p0 + i;
             row_lo = p.win > 0 ? max(0, P - p.win + 1) : 0;
@@ -174,21 +202,23 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             if (p.hi) {
                 hv = p.hi[i];
                 if (hv < P || hv > p.p0 + p.n - 1) {
-                    atomicOr(p.status, WA_STATUS_BAD_HI);
+                    if (warp < 8) atomicOr(p.status, WA_STATUS_BAD_HI);
                     hv = min(max(hv, P), p.p0 + p.n - 1);
                 }
             }
             row_hi = hv;
         }
-        int mn = (i < p.n) ? row_lo : INT_MAX, mx = (i < p.n) ? row_hi : INT_MIN;
+        if (warp < 8) {
+            int mn = (i < p.n) ? row_lo : INT_MAX, mx = (i < p.n) ? row_hi : INT_MIN;
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
-            mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-        }
-        if (lane == 0) {
-            misc[1 + warp - 4] = static_cast<uint32_t>(mn);
-            misc[5 + warp - 4] = static_cast<uint32_t>(mx);
+            for (int off = 16; off >= 1; off >>= 1) {
+                mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
+                mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+            }
+            if (lane == 0) {
+                misc[1 + warp - 4] = static_cast<uint32_t>(mn);
+                misc[5 + warp - 4] = static_cast<uint32_t>(mx);
+            }
         }
     }
     tc_fence_before();
@@ -256,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (one thread)
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(kBM, T, 0, 0);
+            const uint32_t idS = idesc_bf16_f32(kBM, T, 0, 0, p.neg ? 1u : 0u);
             constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
             bool ok = mbar_wait(BAR(B_Q), 0, p.status);
             for (int idx = 0; ok && idx <= ntiles; ++idx) {
@@ -325,43 +355,46 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             if (lane == 0) mbar_arrive(BAR(B_VREADY + s));
         }
     } else if (warp >= 4) {
-        // ------------------------------------------------ softmax, one row per thread
-        const int r = threadIdx.x - 128;
-        const int i = m0 + r;
-        const uint32_t lane_addr = static_cast<uint32_t>((warp - 4) * 32) << 16;
+        // ------------------------------------------------ softmax: row r, column half wg
+        const int wg = (warp - 4) >> 2;
+        const int col0 = wg * NC;                                    // first S column of this half
+        const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const float c = p.c;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int idx = 0; ok && idx < ntiles; ++idx) {
             const int s = idx & 1, u = idx >> 1;
             if (!mbar_wait(BAR(B_SFULL + s), u & 1, p.status)) { ok = false; break; }
             tc_fence_after();
-            float sv[T];
-#pragma unroll
-            for (int c = 0; c < T / 32; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(tbase + lane_addr + C::S_COL + s * T + c * 32, raw);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) sv[c * 32 + e] = __uint_as_float(raw[e]);
-            }
+            float sv[NC];
+            load_s<NC>(tbase + lane_addr + C::S_COL + s * T + col0, sv);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_SFREE + s));
 
-            // mask, scale (log2 units), tile max
-            const int key0 = (j0 + idx) * T;
+            // visible columns of this half: [vlo, vhi]; interior tiles need no mask at all
+            const int kbase = (j0 + idx) * T + col0;
+            const int vlo = row_lo - kbase, vhi = row_hi - kbase;
+            const bool masked = !__all_sync(0xFFFFFFFFu, vlo <= 0 && vhi >= NC - 1);
             float mx8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+            if (masked) {
 #pragma unroll
-            for (int k = 0; k < T; ++k) {
-                const int key = key0 + k;
-                const float x = (key >= row_lo && key <= row_hi) ? sv[k] * p.scale_log2 : -INFINITY;
-                sv[k] = x;
-                mx8[k & 7] = fmaxf(mx8[k & 7], x);
+                for (int k = 0; k < NC; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], (k >= vlo && k <= vhi) ? sv[k] : -INFINITY);
+            } else {
+#pragma unroll
+                for (int k = 0; k < NC; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
             }
-            const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+            const float mh = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            // exchange the half-row maxima (raw S units) with the other half
+            float* xs = xbuf + (idx & 1) * (2 * kBM);
+            xs[wg * kBM + r] = mh;
+            mbar_arrive(BAR(B_XCHG + (idx & 1)));
+            if (!mbar_wait(BAR(B_XCHG + (idx & 1)), (idx >> 1) & 1, p.status)) { ok = false; break; }
+            const float mraw = fmaxf(xs[r], xs[kBM + r]);   // the same order in both halves
+            const float mt = mraw * c;                       // tile max in log2 units
             // lazy rescale: keep the running max unless the tile's exceeds it by more than kLazy
             const float m_new = (mt > m_run + kLazy) ? mt : m_run;
             const float alpha = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
@@ -369,11 +402,20 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             float ls8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) ls8[e] = 0.f;
+            if (masked) {   // a masked column is 0 whatever its score (also for scale 0 or a NaN key)
 #pragma unroll
-            for (int k = 0; k < T; ++k) {
-                const float pk = ex2(sv[k] - m_sub);
-                sv[k] = pk;
-                ls8[k & 7] += pk;
+                for (int k = 0; k < NC; ++k) {
+                    const float pk = (k >= vlo && k <= vhi) ? ex2(fmaf(sv[k], c, -m_sub)) : 0.f;
+                    sv[k] = pk;
+                    ls8[k & 7] += pk;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    const float pk = ex2(fmaf(sv[k], c, -m_sub));
+                    sv[k] = pk;
+                    ls8[k & 7] += pk;
+                }
             }
             const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
             l_run = (alpha == 1.f) ? (l_run + lsum) : fmaf(l_run, alpha, lsum);
@@ -385,11 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
                 tc_fence_after();
                 if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int cc = 0; cc < D / 64; ++cc) {
                         uint32_t o[32];
-                        const uint32_t ta = tbase + lane_addr + C::O_COL + c * 32;
-                        tmem_ld32(ta, o);
-                        tmem_wait_ld();
+                        const uint32_t ta = tbase + lane_addr + C::O_COL + wg * (D / 2) + cc * 32;
+                        tmem_ld32_wait(ta, o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                         tmem_st32(ta, o);
@@ -399,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             }
             // P (and its residual for P32) into the swizzled K-major A tile
 #pragma unroll
-            for (int cb = 0; cb < T / 8; ++cb) {
+            for (int cb = 0; cb < NC / 8; ++cb) {
                 uint32_t w[4], wl[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -410,7 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
                         wl[e] = pack_bf16(a - ah, b - bh);
                     }
                 }
-                const int blk = cb >> 3, c16 = cb & 7;
+                const int kc = col0 / 8 + cb;                    // 8-key chunk index within the tile
+                const int blk = kc >> 3, c16 = kc & 7;
                 const uint32_t off = blk * C::P_BLOCK + r * 128 + ((c16 ^ (r & 7)) * 16);
                 st_shared_v4(sbase + C::OFF_P + off, w[0], w[1], w[2], w[3]);
                 if constexpr (P32) st_shared_v4(sbase + C::OFF_P + C::P_BYTES + off, wl[0], wl[1], wl[2], wl[3]);
@@ -420,31 +462,42 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_PFULL));
         }
-        // epilogue: o = O / l, bf16, non-finite rows go to the float64 re-run
-        if (ok && mbar_wait(BAR(B_PVDONE), (ntiles - 1) & 1, p.status)) {
+        // epilogue: l = l(half 0) + l(half 1); o = O / l, bf16; a non-finite row goes to the float64 re-run
+        if (ok) ok = mbar_wait(BAR(B_PVDONE), (ntiles - 1) & 1, p.status);
+        float* xl = xbuf + ((ntiles & 1) ^ 0) * (2 * kBM);   // the buffer the last tile did not use
+        if (ok) {
+            xl[wg * kBM + r] = l_run;
+            mbar_arrive(BAR(B_EPI_L));
+            ok = mbar_wait(BAR(B_EPI_L), 0, p.status);
+        }
+        if (ok) {
+            const float l = xl[r] + xl[kBM + r];
             tc_fence_after();
             bool bad = false;
-            uint16_t* orow = p.out + static_cast<int64_t>(i) * p.o_tok + static_cast<int64_t>(h) * D;
+            uint16_t* orow = p.out + static_cast<int64_t>(i) * p.o_tok + static_cast<int64_t>(h) * D + wg * (D / 2);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(tbase + lane_addr + C::O_COL + c * 32, o);
-                tmem_wait_ld();
+                tmem_ld32_wait(tbase + lane_addr + C::O_COL + wg * (D / 2) + cc * 32, o);
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float a = __fdiv_rn(__uint_as_float(o[2 * e]), l_run);
-                    const float b = __fdiv_rn(__uint_as_float(o[2 * e + 1]), l_run);
+                    const float a = __fdiv_rn(__uint_as_float(o[2 * e]), l);
+                    const float b = __fdiv_rn(__uint_as_float(o[2 * e + 1]), l);
                     bad |= !(isfinite(a) && isfinite(b));
                     pk[e] = pack_bf16(a, b);
                 }
                 if (i < p.n) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+                    uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                 }
             }
-            if (bad && i < p.n) {
+            // both halves' verdicts meet in the other exchange buffer; half 0 queues the row
+            int* xb = reinterpret_cast<int*>(xbuf + ((ntiles & 1) ^ 1) * (2 * kBM));
+            xb[wg * kBM + r] = bad ? 1 : 0;
+            mbar_arrive(BAR(B_EPI_B));
+            if (mbar_wait(BAR(B_EPI_B), 0, p.status) && wg == 0 && i < p.n && (xb[r] | xb[kBM + r])) {
                 const int slot = atomicAdd(p.nflag, 1);
                 p.flags[slot] = i * p.hq + h;
             }
@@ -501,7 +554,8 @@ cudaError_t launch_t(const PromptArgs& a, cudaStream_t s) {
     pp.o_tok = a.o_tok;
     pp.p0 = a.p0; pp.n = a.n; pp.hq = a.hq; pp.hkv = a.hkv; pp.win = a.win; pp.ring = a.ring;
     pp.nqt = (a.n + kBM - 1) / kBM;
-    pp.scale_log2 = a.scale * 1.4426950408889634f;
+    pp.neg = a.scale < 0.f ? 1 : 0;
+    pp.c = (a.scale < 0.f ? -a.scale : a.scale) * 1.4426950408889634f;
     const dim3 grid(pp.nqt, a.hq);
     prompt_kernel<D, P32><<<grid, kThreads, C::SMEM, s>>>(pp);
     return cudaGetLastError();

@@ -65,10 +65,11 @@ def test_decode_parity(wa, case):
     assert r["n_nonfinite_ref"] == 0
 
 
-def test_decode_scale_parameter(wa):
+@pytest.mark.parametrize("scale", [0.0625, -0.5, 0.0])
+def test_decode_scale_parameter(wa, scale):
     c = _case(3, 16, 8, 256, 1024, 1536, [900, 1700, 2047], seed=3)
-    out = wa.decode(c["q"], c["k"], c["v"], c["pos"], 1024, 0.0625)
-    assert_parity(out, decode_ref(c, scale=0.0625), TOL, "scale")
+    out = wa.decode(c["q"], c["k"], c["v"], c["pos"], 1024, scale)
+    assert_parity(out, decode_ref(c, scale=scale), TOL, f"scale {scale}")
 
 
 def test_batch_composition_and_slot_do_not_change_bits(wa):

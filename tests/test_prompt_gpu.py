@@ -81,10 +81,12 @@ def test_prompt_parity(wa, case):
     assert r["n_nonfinite_ref"] == 0
 
 
-def test_prompt_scale_parameter(wa):
-    c = _case(200, 500, 8, 4, 128, 300, 600, seed=5)
-    out = wa.prompt(c["q"], c["k"], c["v"], 500, None, 300, 0.37, p32=True)
-    assert_parity(out, _ref(c, scale=0.37), check.TOL_P32, "scale")
+@pytest.mark.parametrize("scale", [0.37, -0.5, 0.0])
+@pytest.mark.parametrize("d", [128, 256])
+def test_prompt_scale_parameter(wa, scale, d):
+    c = _case(200, 500, 8, 4, d, 300, 600, seed=5)
+    out = wa.prompt(c["q"], c["k"], c["v"], 500, None, 300, scale, p32=True)
+    assert_parity(out, _ref(c, scale=scale), check.TOL_P32, f"scale {scale}")
 
 
 def test_chunk_split_gives_every_rows_bits(wa):
