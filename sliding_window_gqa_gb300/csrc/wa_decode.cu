@@ -10,9 +10,11 @@
 // the batch, the row's slot or the ring length.
 //
 // GB300 design: the CTA holds every query head of its key-head group, so K
-// and V are read from HBM once per group.  A producer warp stages each
-// visible key row (d*2 bytes) into shared memory with cp.async.bulk (TMA
-// engine) against mbarriers, 32-key runs through a ring of stages; eight
+// and V are read from HBM once per group.  A producer warp stages 32-key runs
+// into a ring of shared-memory stages against mbarriers: a run whose keys are
+// all visible and sit in consecutive ring slots is one TMA tensor box (32 key
+// rows of one head); a run cut by the window or the ring's end is copied row
+// by row with cp.async.bulk.  Eight
 // consumer warps each own one 32-key run of the chunk.  Scores use an fp32
 // fma chain over a lane's d/32 dims, then a butterfly over the 32 lanes
 // (every lane ends with identical bits); o is an fma chain in key order per
@@ -96,9 +98,15 @@ __device__ __forceinline__ int checked_pos(const int32_t* pos, int r, int win, i
     return p;
 }
 
+// K and V rings as 4-D tensors (d, key head, slot, row); one box is one 32-key run of one head.
+struct RingMaps {
+    CUtensorMap tk, tv;
+};
+
 template <int D, int G>
 __global__ void __launch_bounds__(kPartThreads, PartCfg<D, G>::MIN_BLOCKS)
-decode_part_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+decode_part_kernel(const __grid_constant__ RingMaps maps,
+                   const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                    const __nv_bfloat16* __restrict__ v, const int32_t* __restrict__ pos,
                    int hq, int hkv, int gsize, int win, int ring, float scale, int cmax,
                    float* __restrict__ part, int* __restrict__ status) {
@@ -151,11 +159,22 @@ decode_part_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
             const int rb = cbase + run * kRun;
             const int a = max(kb, rb), b = min(ke, rb + kRun - 1);
             const int j = rb + lane;
-            if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * t, static_cast<uint32_t>((b - a + 1) * C::ROWB));
-            __syncwarp();
-            if (j >= a && j <= b) {
-                const __nv_bfloat16* src = src_base + ((row0 + static_cast<size_t>(j % ring)) * hkv + g) * D;
-                bulk_g2s(smem_u32(stage + st * C::STAGE_B + lane * C::ROWB), src, C::ROWB, bar_full + 8 * t, pol);
+            const int slot_rb = rb % ring;
+            if (a == rb && b == rb + kRun - 1 && slot_rb + kRun <= ring) {
+                // a whole run in consecutive slots: one tensor box of 32 key rows
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar_full + 8 * t, static_cast<uint32_t>(kRun * C::ROWB));
+                    tma_load_4d(smem_u32(stage + st * C::STAGE_B), (t < nr) ? &maps.tk : &maps.tv, 0, g, slot_rb, r,
+                                bar_full + 8 * t, pol);
+                }
+            } else {
+                // a run cut by the window or by the end of the ring: one bulk copy per visible key row
+                if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * t, static_cast<uint32_t>((b - a + 1) * C::ROWB));
+                __syncwarp();
+                if (j >= a && j <= b) {
+                    const __nv_bfloat16* src = src_base + ((row0 + static_cast<size_t>(j % ring)) * hkv + g) * D;
+                    bulk_g2s(smem_u32(stage + st * C::STAGE_B + lane * C::ROWB), src, C::ROWB, bar_full + 8 * t, pol);
+                }
             }
             issued = t + 1;
         }
@@ -346,12 +365,30 @@ decode_merge_kernel(const float* __restrict__ part, const int32_t* __restrict__ 
     }
 }
 
+// [rows, ring, hkv, d] bf16 as a 4-D tensor map with a box of d x 1 x 32 x 1 (no swizzle).
+bool encode_ring(CUtensorMap* m, const void* base, int d, int hkv, int ring, int rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(ring),
+                          static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(hkv) * d * 2,
+                             static_cast<cuuint64_t>(ring) * hkv * d * 2};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(d), 1, static_cast<cuuint32_t>(kRun), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int G>
 cudaError_t launch_part(const DecodeArgs& a, cudaStream_t s) {
     using C = PartCfg<D, G>;
+    RingMaps maps;
+    if (!encode_ring(&maps.tk, a.k, D, a.hkv, a.ring, a.rows) || !encode_ring(&maps.tv, a.v, D, a.hkv, a.ring, a.rows))
+        return cudaErrorInvalidValue;
     const dim3 grid(a.cmax, a.hkv, a.rows);
     decode_part_kernel<D, G><<<grid, kPartThreads, C::SMEM, s>>>(
-        static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
+        maps, static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
         static_cast<const __nv_bfloat16*>(a.v), a.pos, a.hq, a.hkv, a.hq / a.hkv, a.win, a.ring, a.scale, a.cmax, a.part,
         &a.hdr->status);
     return cudaGetLastError();

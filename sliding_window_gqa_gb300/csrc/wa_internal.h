@@ -3,6 +3,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 namespace wa {
@@ -63,6 +65,9 @@ struct RerunArgs {
     WsHeader* hdr;
     const int* flags;
 };
+
+// cuTensorMapEncodeTiled from the driver, looked up once; null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_prompt(const PromptArgs& a, cudaStream_t s);

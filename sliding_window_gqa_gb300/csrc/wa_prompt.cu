@@ -511,16 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
 
 cudaError_t get_encoder() {
-    std::call_once(g_encode_once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void* fn = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
+    g_encode = tensor_map_encoder();
     return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
@@ -567,6 +560,19 @@ cudaError_t set_attr() {
 }
 
 }  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn_ptr = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn_ptr = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return fn_ptr;
+}
 
 cudaError_t prompt_prepare_device(int) {
     cudaError_t e;
