@@ -153,7 +153,7 @@ decode_part_kernel(const __grid_constant__ RingMaps maps,
         bool ok = true;
         for (int t = 0; t < 2 * nr; ++t) {
             const int st = t % C::STAGES;
-            if (t >= C::STAGES && !mbar_wait(bar_used + 8 * (t - C::STAGES), 0, status)) { ok = false; break; }
+            if (t >= C::STAGES && !warp_wait(bar_used + 8 * (t - C::STAGES), 0, status)) { ok = false; break; }
             const int run = w0 + (t % nr);
             const __nv_bfloat16* src_base = (t < nr) ? k : v;
             const int rb = cbase + run * kRun;
@@ -213,7 +213,7 @@ decode_part_kernel(const __grid_constant__ RingMaps maps,
     if (active) {
         const int t = w - w0;
         const int st = t % C::STAGES;
-        ok = mbar_wait(bar_full + 8 * t, 0, status);
+        ok = warp_wait(bar_full + 8 * t, 0, status);
         if (ok) {
             const uint8_t* base = stage + st * C::STAGE_B;
             for (int jj = a - rb; jj <= b - rb; ++jj) {
@@ -272,7 +272,7 @@ decode_part_kernel(const __grid_constant__ RingMaps maps,
         __syncwarp();
         const int t = nr + (w - w0);
         const int st = t % C::STAGES;
-        ok = mbar_wait(bar_full + 8 * t, 0, status);
+        ok = warp_wait(bar_full + 8 * t, 0, status);
         if (ok) {
             const uint8_t* base = stage + st * C::STAGE_B;
             for (int jj = a - rb; jj <= b - rb; ++jj) {

@@ -176,13 +176,13 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             mbar_init(BAR(B_VFREE + s), 1);
             mbar_init(BAR(B_SFULL + s), 1);
             mbar_init(BAR(B_SFREE + s), 8);
-            mbar_init(BAR(B_XCHG + s), kSoftmax);
+            mbar_init(BAR(B_XCHG + s), 8);      // one arrival per softmax warp
         }
         mbar_init(BAR(B_PFULL), 8);
         mbar_init(BAR(B_PVDONE), 1);
         mbar_init(BAR(B_DRAIN), 1);
-        mbar_init(BAR(B_EPI_L), kSoftmax);
-        mbar_init(BAR(B_EPI_B), kSoftmax);
+        mbar_init(BAR(B_EPI_L), 8);
+        mbar_init(BAR(B_EPI_B), 8);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             for (int kv = 0; kv < 2 && ok; ++kv) {
                 const uint32_t full = BAR((kv ? B_VFULL : B_KFULL) + s);
                 const uint32_t dst = sbase + (kv ? C::OFF_V : C::OFF_K) + s * C::KV_BYTES;
-                if (u > 0 && !mbar_wait(BAR((kv ? B_VFREE : B_KFREE) + s), (u - 1) & 1, p.status)) {
+                if (u > 0 && !warp_wait(BAR((kv ? B_VFREE : B_KFREE) + s), (u - 1) & 1, p.status)) {
                     ok = false;
                     break;
                 }
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
         // ------------------------------------------------ V rows outside the key union -> 0
         for (int idx = 0; idx < ntiles; ++idx) {
             const int s = idx & 1, u = idx >> 1;
-            if (!mbar_wait(BAR(B_VFULL + s), u & 1, p.status)) break;
+            if (!warp_wait(BAR(B_VFULL + s), u & 1, p.status)) break;
             const int key0 = (j0 + idx) * T;
             const int z_lo = (idx == 0) ? min(T, max(0, ulo - key0)) : 0;            // rows [0, z_lo)
             const int z_hi = (idx == ntiles - 1) ? max(0, min(T, uhi - key0 + 1)) : T; // rows [z_hi, T)
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
         bool ok = true;
         for (int idx = 0; ok && idx < ntiles; ++idx) {
             const int s = idx & 1, u = idx >> 1;
-            if (!mbar_wait(BAR(B_SFULL + s), u & 1, p.status)) { ok = false; break; }
+            if (!warp_wait(BAR(B_SFULL + s), u & 1, p.status)) { ok = false; break; }
             tc_fence_after();
             float sv[NC];
             load_s<NC>(tbase + lane_addr + C::S_COL + s * T + col0, sv);
@@ -391,8 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             // exchange the half-row maxima (raw S units) with the other half
             float* xs = xbuf + (idx & 1) * (2 * kBM);
             xs[wg * kBM + r] = mh;
-            mbar_arrive(BAR(B_XCHG + (idx & 1)));
-            if (!mbar_wait(BAR(B_XCHG + (idx & 1)), (idx >> 1) & 1, p.status)) { ok = false; break; }
+            __syncwarp();   // the warp's stores precede lane 0's (cumulative) release
+            if (lane == 0) mbar_arrive(BAR(B_XCHG + (idx & 1)));
+            if (!warp_wait(BAR(B_XCHG + (idx & 1)), (idx >> 1) & 1, p.status)) { ok = false; break; }
             const float mraw = fmaxf(xs[r], xs[kBM + r]);   // the same order in both halves
             const float mt = mraw * c;                       // tile max in log2 units
             // lazy rescale: keep the running max unless the tile's exceeds it by more than kLazy
@@ -423,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
 
             // the previous P.V must be done before O is rescaled and P is overwritten
             if (idx >= 1) {
-                if (!mbar_wait(BAR(B_PVDONE), (idx - 1) & 1, p.status)) { ok = false; break; }
+                if (!warp_wait(BAR(B_PVDONE), (idx - 1) & 1, p.status)) { ok = false; break; }
                 tc_fence_after();
                 if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
 #pragma unroll 1
@@ -463,12 +464,13 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             if (lane == 0) mbar_arrive(BAR(B_PFULL));
         }
         // epilogue: l = l(half 0) + l(half 1); o = O / l, bf16; a non-finite row goes to the float64 re-run
-        if (ok) ok = mbar_wait(BAR(B_PVDONE), (ntiles - 1) & 1, p.status);
+        if (ok) ok = warp_wait(BAR(B_PVDONE), (ntiles - 1) & 1, p.status);
         float* xl = xbuf + ((ntiles & 1) ^ 0) * (2 * kBM);   // the buffer the last tile did not use
         if (ok) {
             xl[wg * kBM + r] = l_run;
-            mbar_arrive(BAR(B_EPI_L));
-            ok = mbar_wait(BAR(B_EPI_L), 0, p.status);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_EPI_L));
+            ok = warp_wait(BAR(B_EPI_L), 0, p.status);
         }
         if (ok) {
             const float l = xl[r] + xl[kBM + r];
@@ -496,8 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             // both halves' verdicts meet in the other exchange buffer; half 0 queues the row
             int* xb = reinterpret_cast<int*>(xbuf + ((ntiles & 1) ^ 1) * (2 * kBM));
             xb[wg * kBM + r] = bad ? 1 : 0;
-            mbar_arrive(BAR(B_EPI_B));
-            if (mbar_wait(BAR(B_EPI_B), 0, p.status) && wg == 0 && i < p.n && (xb[r] | xb[kBM + r])) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_EPI_B));
+            if (warp_wait(BAR(B_EPI_B), 0, p.status) && wg == 0 && i < p.n && (xb[r] | xb[kBM + r])) {
                 const int slot = atomicAdd(p.nflag, 1);
                 p.flags[slot] = i * p.hq + h;
             }

@@ -70,6 +70,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
     }
 }
 
+// mbar_wait by every lane of a warp, with one verdict for the whole warp, so
+// a wait that runs out never splits the warp before a full-mask warp operation.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* status) {
+    const bool ok = mbar_wait(bar, parity, status);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // ---------------------------------------------------------------------------
 // Bulk copies (TMA engine): untiled 1D and tiled tensor loads into shared memory
 // ---------------------------------------------------------------------------
