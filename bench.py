@@ -389,6 +389,22 @@ def io_bytes(obj) -> int:
     return 0
 
 
+def reduce_max(x: float, dist, device) -> float:
+    """The maximum of x over all ranks (the slowest rank sets the time); x itself with one rank."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(t_roof_s: float, ms_per_step: float, world: int) -> float:
+    """Whole-job fraction of roofline: every rank runs its own copy of the workload (no data exchange),
+    so the job does world x the roofline work in the slowest rank's time."""
+    return t_roof_s * world / (ms_per_step * 1e-3)
+
+
 def run_native(args, parts, rank, world, dist):
     import torch
 
@@ -432,11 +448,7 @@ def run_native(args, parts, rank, world, dist):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(t_start.elapsed_time(t_end), dist, dev)
     ms_per_step = total_ms / args.steps
 
     # e2e: the same step through the C ABI with host buffers (H2D of inputs, D2H of outputs each step)
@@ -454,11 +466,7 @@ def run_native(args, parts, rank, world, dist):
             step(host)
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1) / ksteps
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = reduce_max(e0.elapsed_time(e1) / ksteps, dist, dev)
         h2d = sum(io_bytes({k: v for k, v in h.items() if k != "out"}) if isinstance(h, dict)
                   else sum(io_bytes({k: v for k, v in x.items() if k != "out"}) for x in h) for h in host)
         d2h = sum(io_bytes(h["out"]) if isinstance(h, dict) else sum(io_bytes(x["out"]) for x in h) for h in host)
@@ -617,8 +625,7 @@ def main():
     ms_per_step, per_part_ms, clk, e2e, launches = run_native(args, parts, rank, world, dist)
     pk = peaks()
     t_roof = roofline_seconds(parts, pk)
-    value_one = t_roof / (ms_per_step * 1e-3)
-    value = value_one * world            # every rank runs its own copy of the workload (weak scaling)
+    value = weak_scaling_value(t_roof, ms_per_step, world)
 
     part_report = {}
     for p in parts:
@@ -653,7 +660,7 @@ def main():
         "parts": part_report, "roofline": roof, "clocks": clk, "gpu_launches": launches,
     }
     if e2e is not None:
-        line["e2e"] = {"value": t_roof * world / (e2e["ms_per_step"] * 1e-3), "unit": UNIT,
+        line["e2e"] = {"value": weak_scaling_value(t_roof, e2e["ms_per_step"], world), "unit": UNIT,
                        "h2d_bytes_per_step": e2e["h2d_bytes_per_step"], "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
                        "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"]}
     if rank == 0 and not args.no_cpu_baseline:
