@@ -17,8 +17,8 @@
 //   warp 2      zeroes V rows outside the CTA's key union in the first and
 //               last tile, so stale ring slots never meet a zero P as 0 * inf.
 //   warps 4..7  one query row per thread (= tensor-memory lane): mask, scale,
-//               online softmax with a lazy rescale, P to shared memory as
-//               the A operand of P V, O rescale in tensor memory, epilogue.
+//               online softmax with a lazy rescale, P (bf16) to tensor memory
+//               as the A operand of P V, O rescale in tensor memory, epilogue.
 // Every mbarrier has one waiter role that takes its phases in order.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -62,29 +62,30 @@ struct Cfg {
     static constexpr int Q_BYTES = KB * Q_BLOCK;
     static constexpr int KV_BLOCK = T * 128;
     static constexpr int KV_BYTES = KB * KV_BLOCK;
-    static constexpr int PB = T / 64;
-    static constexpr int P_BLOCK = kBM * 128;
-    static constexpr int P_BYTES = PB * P_BLOCK;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;               // 2 stages
     static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;          // 2 stages
-    static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;          // hi, then lo for P32
-    static constexpr int OFF_X = OFF_P + (P32 ? 2 : 1) * P_BYTES;   // row exchange [2 tiles][2 halves][128] fp32
+    // P lives in tensor memory (the A operand of P.V): two buffers (tiles alternate) for a
+    // single bf16 P, one buffer of two halves (hi, lo) for P32; T / 2 columns each.
+    static constexpr int P_BUFS = P32 ? 1 : 2;
+    static constexpr int OFF_X = OFF_V + 2 * KV_BYTES;          // row exchange [2 tiles][2 halves][128] fp32
     static constexpr int OFF_BAR = OFF_X + 2 * 2 * kBM * 4;
-    static constexpr int NBAR = 22;
+    static constexpr int NBAR = 24;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, union bounds
     static constexpr int SMEM = OFF_MISC + 64;
     static constexpr int TMEM_COLS = 512;
     static constexpr int O_COL = 0;
     static constexpr int S_COL = D;                             // S buffers at D and D + T
-    static_assert(D + 2 * T <= TMEM_COLS, "tensor memory budget");
+    static constexpr int P_COL = D + 2 * T;                     // P: 2 x T/2 columns
+    __host__ __device__ static constexpr int p_col(int buf_or_half) { return P_COL + buf_or_half * (T / 2); }
+    static_assert(D + 3 * T <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 // barrier indices
 enum : int {
     B_Q = 0, B_KFULL = 1, B_VFULL = 3, B_VREADY = 5, B_KFREE = 7, B_VFREE = 9, B_SFULL = 11, B_SFREE = 13,
-    B_PFULL = 15, B_PVDONE = 16, B_DRAIN = 17, B_XCHG = 18, B_EPI_L = 20, B_EPI_B = 21
+    B_PFULL = 15, B_PVDONE = 17, B_DRAIN = 19, B_XCHG = 20, B_EPI_L = 22, B_EPI_B = 23   // PFULL, PVDONE: [tile & 1]
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -178,8 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             mbar_init(BAR(B_SFREE + s), 8);
             mbar_init(BAR(B_XCHG + s), 8);      // one arrival per softmax warp
         }
-        mbar_init(BAR(B_PFULL), 8);
-        mbar_init(BAR(B_PVDONE), 1);
+        mbar_init(BAR(B_PFULL + 0), 8);
+        mbar_init(BAR(B_PFULL + 1), 8);
+        mbar_init(BAR(B_PVDONE + 0), 1);
+        mbar_init(BAR(B_PVDONE + 1), 1);
         mbar_init(BAR(B_DRAIN), 1);
         mbar_init(BAR(B_EPI_L), 8);
         mbar_init(BAR(B_EPI_B), 8);
@@ -308,22 +311,21 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
                 }
                 if (idx >= 1) {
                     const int pidx = idx - 1, ps = pidx & 1, pu = pidx >> 1;
-                    ok = mbar_wait(BAR(B_PFULL), pidx & 1, p.status);
+                    ok = mbar_wait(BAR(B_PFULL + (pidx & 1)), (pidx >> 1) & 1, p.status);
                     if (ok) ok = mbar_wait(BAR(B_VREADY + ps), pu & 1, p.status);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t vst = sbase + C::OFF_V + ps * C::KV_BYTES;
 #pragma unroll
                     for (int half = 0; half < (P32 ? 2 : 1); ++half) {
-                        const uint32_t pbase = sbase + C::OFF_P + half * C::P_BYTES;
+                        const uint32_t pt = tbase + C::p_col(P32 ? half : (pidx & 1));
 #pragma unroll
                         for (int kk = 0; kk < T / 16; ++kk) {
-                            const uint64_t a = sdesc_sw128(pbase + (kk >> 2) * C::P_BLOCK + (kk & 3) * 32, 16, 1024);
                             const uint64_t b = sdesc_sw128(vst + kk * 16 * 128, C::KV_BLOCK, 1024);
-                            mma_bf16_ss(tbase + C::O_COL, a, b, idO, (pidx > 0 || kk > 0 || half > 0) ? 1u : 0u);
+                            mma_bf16_ts(tbase + C::O_COL, pt + kk * 8, b, idO, (pidx > 0 || kk > 0 || half > 0) ? 1u : 0u);
                         }
                     }
-                    mma_commit(BAR(B_PVDONE));
+                    mma_commit(BAR(B_PVDONE + (pidx & 1)));
                     mma_commit(BAR(B_VFREE + ps));
                 }
             }
@@ -422,11 +424,19 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             l_run = (alpha == 1.f) ? (l_run + lsum) : fmaf(l_run, alpha, lsum);
             m_run = m_new;
 
-            // the previous P.V must be done before O is rescaled and P is overwritten
-            if (idx >= 1) {
-                if (!warp_wait(BAR(B_PVDONE), (idx - 1) & 1, p.status)) { ok = false; break; }
+            // P buffer reuse: the P.V that last read it (tile idx - P_BUFS) must be done
+            const int reuse = idx - C::P_BUFS;
+            if (reuse >= 0) {
+                if (!warp_wait(BAR(B_PVDONE + (reuse & 1)), (reuse >> 1) & 1, p.status)) { ok = false; break; }
                 tc_fence_after();
-                if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+            }
+            // an O rescale must wait for the previous tile's P.V (already covered when P_BUFS is 1)
+            if (idx >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+                if (C::P_BUFS == 2) {
+                    if (!warp_wait(BAR(B_PVDONE + ((idx - 1) & 1)), ((idx - 1) >> 1) & 1, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                }
+                {
 #pragma unroll 1
                     for (int cc = 0; cc < D / 64; ++cc) {
                         uint32_t o[32];
@@ -439,32 +449,34 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
                     tmem_wait_st();
                 }
             }
-            // P (and its residual for P32) into the swizzled K-major A tile
+            // P (and its residual for P32) into tensor memory, two bf16 per column, this thread's columns
+            {
+                uint32_t w[NC / 2], wl[NC / 2];
 #pragma unroll
-            for (int cb = 0; cb < NC / 8; ++cb) {
-                uint32_t w[4], wl[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = sv[cb * 8 + 2 * e], b = sv[cb * 8 + 2 * e + 1];
+                for (int e = 0; e < NC / 2; ++e) {
+                    const float a = sv[2 * e], b = sv[2 * e + 1];
                     w[e] = pack_bf16(a, b);
                     if constexpr (P32) {
                         const float ah = __uint_as_float(w[e] << 16), bh = __uint_as_float(w[e] & 0xFFFF0000u);
                         wl[e] = pack_bf16(a - ah, b - bh);
                     }
                 }
-                const int kc = col0 / 8 + cb;                    // 8-key chunk index within the tile
-                const int blk = kc >> 3, c16 = kc & 7;
-                const uint32_t off = blk * C::P_BLOCK + r * 128 + ((c16 ^ (r & 7)) * 16);
-                st_shared_v4(sbase + C::OFF_P + off, w[0], w[1], w[2], w[3]);
-                if constexpr (P32) st_shared_v4(sbase + C::OFF_P + C::P_BYTES + off, wl[0], wl[1], wl[2], wl[3]);
+                const uint32_t pa = tbase + lane_addr + C::p_col(P32 ? 0 : (idx & 1)) + col0 / 2;
+                if constexpr (NC == 64) {
+                    tmem_st32(pa, w);
+                    if constexpr (P32) tmem_st32(tbase + lane_addr + C::p_col(1) + col0 / 2, wl);
+                } else {
+                    tmem_st16(pa, w);
+                    if constexpr (P32) tmem_st16(tbase + lane_addr + C::p_col(1) + col0 / 2, wl);
+                }
+                tmem_wait_st();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_PFULL));
+            if (lane == 0) mbar_arrive(BAR(B_PFULL + (idx & 1)));
         }
         // epilogue: l = l(half 0) + l(half 1); o = O / l, bf16; a non-finite row goes to the float64 re-run
-        if (ok) ok = warp_wait(BAR(B_PVDONE), (ntiles - 1) & 1, p.status);
+        if (ok) ok = warp_wait(BAR(B_PVDONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, p.status);
         float* xl = xbuf + ((ntiles & 1) ^ 0) * (2 * kBM);   // the buffer the last tile did not use
         if (ok) {
             xl[wg * kBM + r] = l_run;
