@@ -94,6 +94,23 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Two fp32 fused multiply-adds (d = a * b + c, round to nearest) in one packed instruction.
+__device__ __forceinline__ void fma_x2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                       float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// Two fp32 additions (round to nearest) in one packed instruction: (s0, s1) += (a0, a1).
+__device__ __forceinline__ void add_x2(float& s0, float& s1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, rs;\n\t"
+        "mov.b64 rs, {%0, %1};\n\tmov.b64 ra, {%2, %3};\n\t"
+        "add.rn.f32x2 rs, rs, ra;\n\tmov.b64 {%0, %1}, rs;\n\t}"
+        : "+f"(s0), "+f"(s1) : "f"(a0), "f"(a1));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -412,12 +429,15 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
                     sv[k] = pk;
                     ls8[k & 7] += pk;
                 }
-            } else {
+            } else {   // two columns per packed FMA and packed add
 #pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    const float pk = ex2(fmaf(sv[k], c, -m_sub));
-                    sv[k] = pk;
-                    ls8[k & 7] += pk;
+                for (int k = 0; k < NC; k += 2) {
+                    float x0, x1;
+                    fma_x2(x0, x1, sv[k], sv[k + 1], c, c, -m_sub, -m_sub);
+                    sv[k] = ex2(x0);
+                    sv[k + 1] = ex2(x1);
+                    const int j = (k >> 1) & 3;
+                    add_x2(ls8[2 * j], ls8[2 * j + 1], sv[k], sv[k + 1]);
                 }
             }
             const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
