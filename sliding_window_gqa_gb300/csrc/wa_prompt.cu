@@ -94,6 +94,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// max of three fp32 values in one instruction (a NaN input is passed over, as by fmaxf).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Two fp32 fused multiply-adds (d = a * b + c, round to nearest) in one packed instruction.
 __device__ __forceinline__ void fma_x2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
                                        float c1) {
@@ -403,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
                 for (int k = 0; k < NC; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], (k >= vlo && k <= vhi) ? sv[k] : -INFINITY);
             } else {
 #pragma unroll
-                for (int k = 0; k < NC; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
+                for (int k = 0; k < NC; k += 2) mx8[(k >> 1) & 7] = max3(mx8[(k >> 1) & 7], sv[k], sv[k + 1]);
             }
             const float mh = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
