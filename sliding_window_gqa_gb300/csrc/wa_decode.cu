@@ -415,7 +415,8 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
     const int G = a.hq / a.hkv;
     cudaError_t e;
     if (G < 1 || G > 16) return cudaErrorInvalidValue;
-    if (G == 1) e = launch_part<D, 1>(a, s);
+    if (G >= kTcMinGroup) e = launch_decode_tc_part(a, s);
+    else if (G == 1) e = launch_part<D, 1>(a, s);
     else if (G == 2) e = launch_part<D, 2>(a, s);
     else if (G <= 4) e = launch_part<D, 4>(a, s);
     else if (G <= 8) e = launch_part<D, 8>(a, s);
@@ -428,10 +429,11 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t decode_prepare_device(int) {
+cudaError_t decode_prepare_device(int dev) {
     cudaError_t e = prepare_d<128>();
     if (e != cudaSuccess) return e;
-    return prepare_d<256>();
+    if ((e = prepare_d<256>()) != cudaSuccess) return e;
+    return decode_tc_prepare_device(dev);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {

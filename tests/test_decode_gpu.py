@@ -51,6 +51,14 @@ CASES = [
     ("gqa16_d128", 17, 32, 2, 128, 1024, 1536, list(range(100, 40000, 2350))[:17]),
     ("one_key_window", 2, 4, 2, 256, 1, 4, [0, 17]),
     ("chunk_edges", 6, 4, 2, 256, 513, 1024, [255, 256, 511, 512, 767, 768]),
+    # groups of 4 and more run on the tensor cores
+    ("gqa4_ring1000_wrap", 4, 16, 4, 256, 700, 1000, [0, 255, 256, 5000]),
+    ("gqa8_linear_d256", 3, 16, 2, 256, 0, 2000, [0, 1023, 1999]),
+    ("gqa4_d128_chunk_edges", 6, 8, 2, 128, 513, 1024, [255, 256, 511, 512, 767, 768]),
+    ("gqa16_one_key_window", 2, 16, 1, 256, 1, 4, [0, 17]),
+    ("gqa8_d128_ring333", 2, 8, 1, 128, 300, 333, [299, 1234]),
+    ("gqa5_d256", 3, 10, 2, 256, 1024, 1536, [1536, 77, 30000]),
+    ("gqa16_d128_many_units", 40, 32, 2, 128, 1024, 1100, list(range(3, 40000, 997))[:40]),
 ]
 
 
@@ -65,16 +73,18 @@ def test_decode_parity(wa, case):
     assert r["n_nonfinite_ref"] == 0
 
 
+@pytest.mark.parametrize("hkv", [8, 2])
 @pytest.mark.parametrize("scale", [0.0625, -0.5, 0.0])
-def test_decode_scale_parameter(wa, scale):
-    c = _case(3, 16, 8, 256, 1024, 1536, [900, 1700, 2047], seed=3)
+def test_decode_scale_parameter(wa, scale, hkv):
+    c = _case(3, 16, hkv, 256, 1024, 1536, [900, 1700, 2047], seed=3)
     out = wa.decode(c["q"], c["k"], c["v"], c["pos"], 1024, scale)
     assert_parity(out, decode_ref(c, scale=scale), TOL, f"scale {scale}")
 
 
-def test_batch_composition_and_slot_do_not_change_bits(wa):
+@pytest.mark.parametrize("hkv", [8, 2, 1])
+def test_batch_composition_and_slot_do_not_change_bits(wa, hkv):
     pos = [40000, 5, 1023, 1024, 7777]
-    c = _case(5, 16, 8, 256, 1024, 1536, pos, seed=8)
+    c = _case(5, 16, hkv, 256, 1024, 1536, pos, seed=8)
     full = wa.decode(c["q"], c["k"], c["v"], c["pos"], 1024, 1.0)
     for order in ([4, 3, 2, 1, 0], [2], [0, 4], [1, 3]):
         sel = torch.tensor(order, device="cuda")
@@ -83,9 +93,10 @@ def test_batch_composition_and_slot_do_not_change_bits(wa):
         assert torch.equal(part.view(torch.int16), full[sel].view(torch.int16)), order
 
 
-def test_linear_cache_declared_16x_longer_gives_same_bits(wa):
+@pytest.mark.parametrize("hq", [8, 32])
+def test_linear_cache_declared_16x_longer_gives_same_bits(wa, hq):
     pos = [0, 700, 1999]
-    c = _case(3, 8, 4, 128, 0, 2000, pos, seed=9)
+    c = _case(3, hq, 4, 128, 0, 2000, pos, seed=9)
     a = wa.decode(c["q"], c["k"], c["v"], c["pos"], 0, 1.0)
     k16 = torch.zeros((3, 32000, 4, 128), dtype=torch.bfloat16, device="cuda")
     v16 = torch.zeros_like(k16)
@@ -105,8 +116,8 @@ def test_repeats_are_byte_identical(wa):
 
 # --------------------------- special values (gate 1 plants) ---------------------------
 
-def _nonfinite_case(mutate):
-    c = wa_synth.decode_case(3, 4, 2, 256, 600, 1024, [700, 1500, 599], seed=12, outside="keep")
+def _nonfinite_case(mutate, hq=4):
+    c = wa_synth.decode_case(3, hq, 2, 256, 600, 1024, [700, 1500, 599], seed=12, outside="keep")
     q, k, v = bits(c["q"]).copy(), bits(c["k"]).copy(), bits(c["v"]).copy()
     mutate(q, k, v)
     dev = {n: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda() for n, x in (("q", q), ("k", k), ("v", v))}
@@ -115,8 +126,9 @@ def _nonfinite_case(mutate):
     return dev, pos, ref
 
 
+@pytest.mark.parametrize("hq", [4, 16])
 @pytest.mark.parametrize("plant", ["nan_query", "nan_key", "inf_value", "pm_inf_column", "inf_at_tiny_weight"])
-def test_nonfinite_classes_match_float64(wa, plant):
+def test_nonfinite_classes_match_float64(wa, plant, hq):
     def mutate(q, k, v):
         if plant == "nan_query":
             q[1, 3, 7] = 0x7FC0
@@ -133,7 +145,7 @@ def test_nonfinite_classes_match_float64(wa, plant):
             big = oracle.f64_to_bf16(qv * (200.0 / float(qv @ qv)))
             k[0, 690 % 1024, 0] = big
             v[0, 300 % 1024, 0, 11] = 0x7F80                 # weight near e^-200 in float64, 0 in fp32
-    dev, pos, ref = _nonfinite_case(mutate)
+    dev, pos, ref = _nonfinite_case(mutate, hq)
     out = wa.decode(dev["q"], dev["k"], dev["v"], pos, 600, 1.0)
     r = assert_parity(out, ref, TOL, plant)
     assert r["n_nonfinite_ref"] > 0
@@ -170,6 +182,32 @@ def test_decode_at_scale_three_streams_sampled(wa):
         ref = decode_ref(c, rows=rows)
         assert_parity(out[rows], ref, TOL, "at scale")
         assert torch.isfinite(out.float()).all()
+
+
+def test_decode_gqa8_at_scale_sampled(wa):
+    """64 rows, 32 query heads over 4 key heads (tensor-core path), d 256, window 1024 over 1536."""
+    gen = torch.Generator().manual_seed(20260005)
+    pos = torch.randint(0, 40001, (64,), generator=gen).tolist()
+    pos[0] = 40000
+    c = wa_synth.decode_case(64, 32, 4, 256, 1024, 1536, pos, seed=20260050, device="cuda", outside="keep")
+    out = wa.decode(c["q"], c["k"], c["v"], c["pos"], 1024, 1.0)
+    torch.cuda.synchronize()
+    rows = [0, 9, 33, 63]
+    assert_parity(out[rows], decode_ref(c, rows=rows), TOL, "gqa8 at scale")
+    assert torch.isfinite(out.float()).all()
+
+
+def test_decode_gqa16_linear_32768_sampled(wa):
+    """64 rows over a linear cache of 32,768 keys, 32 query heads over 2 key heads (tensor-core path)."""
+    gen = torch.Generator().manual_seed(20260006)
+    pos = torch.randint(0, 32768, (64,), generator=gen).tolist()
+    pos[7] = 32767
+    c = wa_synth.decode_case(64, 32, 2, 256, 0, 32768, pos, seed=20260060, device="cuda", outside="keep")
+    out = wa.decode(c["q"], c["k"], c["v"], c["pos"], 0, 1.0)
+    torch.cuda.synchronize()
+    rows = [7, 40]
+    assert_parity(out[rows], decode_ref(c, rows=rows), TOL, "gqa16 linear 32768")
+    assert torch.isfinite(out.float()).all()
 
 
 def test_decode_linear_32768_sampled(wa):
