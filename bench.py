@@ -12,6 +12,11 @@ Numerical Contract" page, "Canonical Boundary"):
   prompt_dense    37,810 rows, 56 heads (MHA), d 128, interleaved QKV (row 21,504),
                   RMSNormed Q/K, scale 1/sqrt(128), non-causal (hi = N-1), bf16 P
 
+Two more decode parts run only when named with --parts (they are not in the
+default step): decode_gqa8 (decode_sliding with 32 query heads over 4 key
+heads) and decode_gqa16_linear (decode_linear with 32 over 2), the groups the
+tensor-core decode serves.
+
 value = (decode bytes / HBM peak + prompt flops / bf16 peak) / measured step time:
 the step's roofline time over its measured time.  Decode bytes are the visible
 K and V rows plus q and out; prompt flops are 4*d per visible (row, key, head).
@@ -43,12 +48,16 @@ UNIT = "fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 PARTS = ("decode_sliding", "decode_linear", "prompt_causal", "prompt_dense")
+EXTRA_PARTS = ("decode_gqa8", "decode_gqa16_linear")
 SPEC = {
     "decode_sliding": dict(caches=3, rows=64, hq=32, hkv=16, d=256, win=1024, ring=1536, pos_max=40000,
                            seed=20260003),
     "decode_linear": dict(rows=64, hq=32, hkv=16, d=256, win=0, ring=32768, seed=20260004),
     "prompt_causal": dict(n=8192, p0=0, hq=16, hkv=8, d=256, win=0, ring=8192, p32=True, seed=20260005),
     "prompt_dense": dict(N=37810, H=56, d=128, p32=False, seed=20260006),
+    "decode_gqa8": dict(caches=3, rows=64, hq=32, hkv=4, d=256, win=1024, ring=1536, pos_max=40000,
+                        seed=20260007),
+    "decode_gqa16_linear": dict(rows=64, hq=32, hkv=2, d=256, win=0, ring=32768, seed=20260008),
 }
 
 # ncu DRAM bytes per launch of the dominant kernels, valid only while the kernel source is unchanged.
@@ -64,7 +73,7 @@ def decode_positions(part: str):
     import torch
     s = SPEC[part]
     g = torch.Generator().manual_seed(s["seed"])
-    if part == "decode_sliding":
+    if "caches" in s:
         out = []
         for _ in range(s["caches"]):
             p = torch.randint(0, s["pos_max"] + 1, (s["rows"],), generator=g).tolist()
@@ -362,14 +371,26 @@ class PromptDense(Part):
                 "out": torch_empty_pinned_like(self.out)}
 
 
+class DecodeGqa8(DecodeSliding):
+    name = "decode_gqa8"
+
+
+class DecodeGqa16Linear(DecodeLinear):
+    name = "decode_gqa16_linear"
+
+
 PART_CLASSES = {"decode_sliding": DecodeSliding, "decode_linear": DecodeLinear,
-                "prompt_causal": PromptCausal, "prompt_dense": PromptDense}
+                "prompt_causal": PromptCausal, "prompt_dense": PromptDense,
+                "decode_gqa8": DecodeGqa8, "decode_gqa16_linear": DecodeGqa16Linear}
 
 KERNEL_OF = {"decode_sliding": "decode partial (wa_decode.cu)", "decode_linear": "decode partial (wa_decode.cu)",
              "prompt_causal": "prompt tensor-core tile (wa_prompt.cu)",
-             "prompt_dense": "prompt tensor-core tile (wa_prompt.cu)"}
+             "prompt_dense": "prompt tensor-core tile (wa_prompt.cu)",
+             "decode_gqa8": "tensor-core decode partial (wa_decode_tc.cu)",
+             "decode_gqa16_linear": "tensor-core decode partial (wa_decode_tc.cu)"}
 SOURCE_OF = {"decode_sliding": "wa_decode.cu", "decode_linear": "wa_decode.cu",
-             "prompt_causal": "wa_prompt.cu", "prompt_dense": "wa_prompt.cu"}
+             "prompt_causal": "wa_prompt.cu", "prompt_dense": "wa_prompt.cu",
+             "decode_gqa8": "wa_decode_tc.cu", "decode_gqa16_linear": "wa_decode_tc.cu"}
 
 
 def source_hash(fname: str) -> str:
@@ -617,7 +638,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--parts", default="all", help="comma list of " + ",".join(PARTS))
+    ap.add_argument("--parts", default="all", help="comma list of " + ",".join(PARTS + EXTRA_PARTS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -633,7 +654,7 @@ def main():
     args.warmup = max(args.warmup, 3)
     parts = list(PARTS) if args.parts == "all" else [p for p in args.parts.split(",") if p]
     for p in parts:
-        if p not in PARTS:
+        if p not in PARTS and p not in EXTRA_PARTS:
             raise SystemExit(f"unknown part {p}")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
