@@ -62,8 +62,12 @@ SPEC = {
 
 # ncu DRAM bytes per launch of the dominant kernels, valid only while the kernel source is unchanged.
 TRAFFIC = {
-    "prompt_dense": {"bytes_per_launch": 2070 * 10**6, "source_sha": "88b8ed8aad5d473d",
-                     "note": "ncu at N=8192 (353.0 MB read + 95.5 MB write), scaled by N to 37,810"},
+    "prompt_dense": {"bytes_per_launch": 2070 * 10**6, "source_sha": "1e0dfa0763edd056",
+                     "note": "ncu at N=8192 (352.4 MB read + 96.1 MB write), scaled by N to 37,810"},
+    "decode_gqa8": {"bytes_per_launch": 853 * 10**6, "source_sha": "2033d7ed7d9eaec4",
+                    "note": "the part's three launches together, like its achieved figure: ncu at 256 rows, one cache "
+                            "(1.134 GB read + 8.0 MB write for 1.072 GB algorithmic), scaled by algorithmic bytes "
+                            "to the part's 801 MB"},
 }
 
 
@@ -646,11 +650,16 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="oracle seconds for cpu_baseline")
     ap.add_argument("--caches", type=int, default=None, help="override the decode_sliding cache count (profiling)")
     ap.add_argument("--dense-n", type=int, default=None, help="override the prompt_dense row count (profiling)")
+    ap.add_argument("--decode-rows", type=int, default=None, help="override every decode part's rows per cache (profiling)")
     args = ap.parse_args()
     if args.caches is not None:
         SPEC["decode_sliding"]["caches"] = args.caches
     if args.dense_n is not None:
         SPEC["prompt_dense"]["N"] = args.dense_n
+    if args.decode_rows is not None:
+        for name, sp in SPEC.items():
+            if name.startswith("decode"):
+                sp["rows"] = args.decode_rows
     args.warmup = max(args.warmup, 3)
     parts = list(PARTS) if args.parts == "all" else [p for p in args.parts.split(",") if p]
     for p in parts:
