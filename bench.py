@@ -15,7 +15,9 @@ Numerical Contract" page, "Canonical Boundary"):
 Two more decode parts run only when named with --parts (they are not in the
 default step): decode_gqa8 (decode_sliding with 32 query heads over 4 key
 heads) and decode_gqa16_linear (decode_linear with 32 over 2), the groups the
-tensor-core decode serves.
+tensor-core decode serves.  prep_dense (optional too) is the dense workload's
+q/k preparation: per-head RMSNorm of Q and K in place in the interleaved QKV
+buffer (37,810 tokens, 56 heads, d 128), HBM-bound.
 
 value = (decode bytes / HBM peak + prompt flops / bf16 peak) / measured step time:
 the step's roofline time over its measured time.  Decode bytes are the visible
@@ -48,7 +50,7 @@ UNIT = "fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 PARTS = ("decode_sliding", "decode_linear", "prompt_causal", "prompt_dense")
-EXTRA_PARTS = ("decode_gqa8", "decode_gqa16_linear")
+EXTRA_PARTS = ("decode_gqa8", "decode_gqa16_linear", "prep_dense")
 SPEC = {
     "decode_sliding": dict(caches=3, rows=64, hq=32, hkv=16, d=256, win=1024, ring=1536, pos_max=40000,
                            seed=20260003),
@@ -58,6 +60,7 @@ SPEC = {
     "decode_gqa8": dict(caches=3, rows=64, hq=32, hkv=4, d=256, win=1024, ring=1536, pos_max=40000,
                         seed=20260007),
     "decode_gqa16_linear": dict(rows=64, hq=32, hkv=2, d=256, win=0, ring=32768, seed=20260008),
+    "prep_dense": dict(N=37810, H=56, d=128, seed=20260009),
 }
 
 # ncu DRAM bytes per launch of the dominant kernels, valid only while the kernel source is unchanged.
@@ -115,6 +118,9 @@ def part_work(part: str):
     if part.startswith("decode"):
         return {"bytes": sum(decode_bytes(p, s["hq"], s["hkv"], s["d"], s["win"]) for p in decode_positions(part)),
                 "flops": 0}
+    if part == "prep_dense":
+        # Q and K heads read once and written once (V stays in place)
+        return {"bytes": 2 * s["N"] * 2 * s["H"] * s["d"] * 2, "flops": 0}
     if part == "prompt_causal":
         n = s["n"]
         vis = n * (n + 1) // 2          # row i sees keys 0..i
@@ -375,6 +381,40 @@ class PromptDense(Part):
                 "out": torch_empty_pinned_like(self.out)}
 
 
+class PrepDense(Part):
+    name = "prep_dense"
+
+    def __init__(self, torch, wa, wa_synth, dev):
+        s = SPEC[self.name]
+        self.torch, self.wa = torch, wa
+        N, H, d = s["N"], s["H"], s["d"]
+        W = 3 * H * d
+        g = torch.Generator(device=dev).manual_seed(s["seed"])
+        self.qkv = torch.randn((N, W), generator=g, device=dev).to(torch.bfloat16)   # projection rows
+        self.q = self.qkv.as_strided((N, H, d), (W, d, 1), 0)
+        self.k = self.qkv.as_strided((N, H, d), (W, d, 1), H * d)
+        self.pos = torch.arange(N, dtype=torch.int32, device=dev)
+        self.ws = torch.empty(256, dtype=torch.uint8, device=dev)
+        self.launches = 1
+        self.k_start, self.k_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.kernel_ms = []
+
+    def run(self, stream, host=None):
+        if host is not None:
+            self.qkv.copy_(host["qkv"], non_blocking=True)
+        self.k_start.record(stream)
+        self.wa.prep_append(self.qkv, self.pos, self.q, self.k, None, mode="rmsnorm", ws=self.ws, stream=stream)
+        self.k_end.record(stream)
+        if host is not None:
+            host["out"].copy_(self.qkv, non_blocking=True)
+
+    def collect(self):
+        self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
+
+    def host_buffers(self):
+        return {"qkv": self.qkv.cpu().pin_memory(), "out": torch_empty_pinned_like(self.qkv)}
+
+
 class DecodeGqa8(DecodeSliding):
     name = "decode_gqa8"
 
@@ -385,16 +425,18 @@ class DecodeGqa16Linear(DecodeLinear):
 
 PART_CLASSES = {"decode_sliding": DecodeSliding, "decode_linear": DecodeLinear,
                 "prompt_causal": PromptCausal, "prompt_dense": PromptDense,
-                "decode_gqa8": DecodeGqa8, "decode_gqa16_linear": DecodeGqa16Linear}
+                "decode_gqa8": DecodeGqa8, "decode_gqa16_linear": DecodeGqa16Linear, "prep_dense": PrepDense}
 
 KERNEL_OF = {"decode_sliding": "decode partial (wa_decode.cu)", "decode_linear": "decode partial (wa_decode.cu)",
              "prompt_causal": "prompt tensor-core tile (wa_prompt.cu)",
              "prompt_dense": "prompt tensor-core tile (wa_prompt.cu)",
              "decode_gqa8": "tensor-core decode partial (wa_decode_tc.cu)",
-             "decode_gqa16_linear": "tensor-core decode partial (wa_decode_tc.cu)"}
+             "decode_gqa16_linear": "tensor-core decode partial (wa_decode_tc.cu)",
+             "prep_dense": "q/k preparation (wa_prep.cu)"}
 SOURCE_OF = {"decode_sliding": "wa_decode.cu", "decode_linear": "wa_decode.cu",
              "prompt_causal": "wa_prompt.cu", "prompt_dense": "wa_prompt.cu",
-             "decode_gqa8": "wa_decode_tc.cu", "decode_gqa16_linear": "wa_decode_tc.cu"}
+             "decode_gqa8": "wa_decode_tc.cu", "decode_gqa16_linear": "wa_decode_tc.cu",
+             "prep_dense": "wa_prep.cu"}
 
 
 def source_hash(fname: str) -> str:
@@ -525,6 +567,10 @@ def _sample_inputs(part: str, i: int = 0):
             c = wa_synth.decode_case(1, s["hq"], s["hkv"], s["d"], s["win"], s["ring"], [p],
                                      seed=s["seed"] + i, outside="keep", peaked=False)
             _SAMPLES[key] = (p, bits(c["q"]), bits(c["k"]), bits(c["v"]))
+        elif part == "prep_dense":
+            g = torch.Generator().manual_seed(s["seed"])
+            x = torch.randn((1024, 3 * s["H"] * s["d"]), generator=g).to(torch.bfloat16)
+            _SAMPLES[key] = (bits(x),)
         elif part == "prompt_causal":
             c = wa_synth.prompt_case(s["n"], s["p0"], s["hq"], s["hkv"], s["d"], s["win"], s["ring"], seed=s["seed"],
                                      outside="keep", peaked=False)
@@ -561,6 +607,17 @@ def oracle_sample(parts, budget_s: float):
                 rows_done += 1
             total += t_used * w["bytes"] / work_done
             desc.append(f"{part}: {rows_done} rows of {n_rows}")
+        elif part == "prep_dense":
+            from oracle import prep
+            (x,) = _sample_inputs(part)
+            rows_done, t_used = 0, 0.0
+            while t_used < per and rows_done < s["N"]:
+                t0 = time.perf_counter()
+                prep.prepare(x, np.arange(x.shape[0]), s["H"], s["H"], s["d"], "rmsnorm")
+                t_used += time.perf_counter() - t0
+                rows_done += x.shape[0]
+            total += t_used * s["N"] / rows_done
+            desc.append(f"{part}: {rows_done} tokens of {s['N']}")
         elif part == "prompt_causal":
             n = s["n"]
             q, k, v = _sample_inputs(part)

@@ -49,7 +49,7 @@ extern "C" {
 /* Size of the library-owned scratch array behind wa_decode_static (16 MiB per device). */
 #define WA_STATIC_WS_BYTES (16u * 1024u * 1024u)
 
-#define WA_STATUS_BAD_POS 1   /* a decode pos was < 0, or >= ring with win = 0 (clamped) */
+#define WA_STATUS_BAD_POS 1   /* a decode pos was < 0, or >= ring with win = 0 (clamped); an append pos < 0 (skipped) */
 #define WA_STATUS_BAD_HI 2    /* a prompt hi[i] was outside [p0+i, p0+n-1] (clamped) */
 #define WA_STATUS_TIMEOUT 4   /* a bounded device wait gave up; outputs are not valid */
 #define WA_STATUS_LAYOUT 8    /* a kernel found its shared memory misaligned and wrote nothing */
@@ -142,6 +142,58 @@ int wa_prompt(const void* q, const void* k, const void* v, int32_t p0, int32_t n
               const int32_t* hi, int32_t hq, int32_t hkv, int32_t d, int32_t win, int32_t ring,
               float scale, int32_t p32, const wa_strides* strides, void* out,
               void* ws, size_t ws_bytes, void* stream);
+
+/* Preparations for wa_prep_append. */
+#define WA_PREP_RMSNORM 1     /* per-head RMSNorm of q and k */
+#define WA_PREP_L2_ROPE 2     /* rotate-half RoPE, L2 norm, q scale */
+
+/* Workspace bytes wa_prep_append needs: the 256-byte header (status word). */
+#define WA_PREP_WS_BYTES 256u
+
+/* Layout of wa_prep_append, strides in elements (the head stride is always d). */
+typedef struct wa_prep_layout {
+    int64_t src_tok;    /* between consecutive tokens' projection rows */
+    int64_t q_tok;      /* between consecutive tokens' rows of q_out */
+    int64_t ring_row;   /* between the rings of consecutive tokens; 0 = one shared ring */
+    int64_t slot;       /* between consecutive slots of a ring */
+} wa_prep_layout;
+
+/*
+ * q/k preparation and KV append: the step that feeds the caches wa_decode and
+ * wa_prompt read.  For each of n tokens, src holds hq query heads, then hkv key
+ * heads, then hkv value heads, d bf16 values each (the interleaved projection
+ * row of page "Exact Numerical Contract", section "Canonical Boundary").
+ *
+ *   mode WA_PREP_RMSNORM (page "Exact Numerical Contract", section
+ *     "Preparation"): q and k heads become x / sqrt(mean(x^2) + 1e-5),
+ *     computed in fp32 and rounded once to bf16 RN.
+ *   mode WA_PREP_L2_ROPE (TensorFold pull request #1257, section "What the
+ *     kernel computes"): rotate-half RoPE in fp32 (dimension j < d/2 pairs with
+ *     j + d/2; angle fl32(pos * inv_freq[j]), fp32 cosf/sinf), rounded to bf16;
+ *     then x * (1 / sqrt(sum(x^2) + 1e-6)), rounded to bf16; q heads are then
+ *     multiplied by q_scale[j] in fp32 and rounded to bf16.
+ *
+ *   src      [n] rows of (hq + 2 hkv) * d bf16, token stride lay->src_tok
+ *   pos      [n] int32, device: the token's position; a negative position is
+ *            reported (WA_STATUS_BAD_POS) and that token is not written
+ *   q_scale  [d] fp32, device, or NULL (1.0); WA_PREP_L2_ROPE only
+ *   inv_freq [d/2] fp32, device; required for WA_PREP_L2_ROPE, ignored otherwise
+ *   q_out    prepared q: token t's head h at q_out + t*q_tok + h*d
+ *   k_ring   prepared k: key head g of token t at
+ *            k_ring + t*ring_row + (pos[t] mod ring)*slot + g*d
+ *   v_ring   v copied as is, same addressing; NULL when v already sits there
+ *   ws       WA_PREP_WS_BYTES of device memory, 256-byte aligned (status word)
+ *
+ * q_out and k_ring may be the very src locations they replace (an in-place
+ * preparation of an interleaved buffer, with slot = src_tok and pos[t] = t);
+ * any other overlap is undefined.  Constraints: d in {128, 256}; hq % hkv == 0
+ * and hq / hkv <= 16; n >= 1; ring >= 1; pointers 16-byte aligned, strides
+ * multiples of 8 elements.  Returns WA_EINVAL otherwise.
+ */
+int wa_prep_append(const void* src, const int32_t* pos, int32_t n, int32_t hq, int32_t hkv, int32_t d,
+                   int32_t mode, const float* q_scale, const float* inv_freq, int32_t ring,
+                   const wa_prep_layout* lay, void* q_out, void* k_ring, void* v_ring,
+                   void* ws, size_t ws_bytes, void* stream);
 
 /* Waits for `stream`, then returns the WA_STATUS_* bits the last call that
  * used `ws` left (0 when clean), or a negative WA_E* code if the read fails. */

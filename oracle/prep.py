@@ -25,6 +25,16 @@ q and k and writes k and v into ring slot pos mod ring.  Two preparations:
   that fp32 angle.  Every other step is float64, with bf16 rounding (this
   package's own round-to-nearest-even) at the three points.
 
+  Allowance (the pages compare "with float64's range at its rounding points
+  (cosf's ulps on the fp32 angle)").  An fp32 rotation with cosf/sinf within
+  2 ulps, two rounded products and a rounded difference is within
+  2^-21 (|x_a cos| + |x_b sin|) of the float64 rotation.  Where the two terms
+  cancel, that is many bf16 steps of the rotated value, and it reaches the
+  output scaled by the normalisation (and q_scale).  So each output j is
+  allowed |o_j| 2^-6 (one bf16 step at each earlier rounding point) plus
+  s_j (e_j + ulp_bf16(|r_j| + e_j)) / N, with e_j the rotation bound, r_j the
+  rotated value, N the head's norm and s_j the q scale (1 for k).
+
 v is copied as is.  Reading of "rotate-half": dimension j < d/2 pairs with
 j + d/2; x'_j = x_j cos - x_{j+d/2} sin and x'_{j+d/2} = x_{j+d/2} cos +
 x_j sin, with the angle of frequency j.
@@ -85,43 +95,78 @@ def _rn(x):
     return bf16_to_f64(f64_to_bf16(x))
 
 
-def prepare(src_bits, pos, hq: int, hkv: int, d: int, mode: str, q_scale=None, inv_freq=None):
+def _ulp_bf16(a):
+    """Spacing of bf16 values at magnitude a (normal range)."""
+    e = np.floor(np.log2(np.maximum(np.abs(a), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def _rotation_bound(x, ang):
+    """Bound on |fp32 rotation - float64 rotation| per output dimension (see the module text)."""
+    h = x.shape[-1] // 2
+    c, s = np.abs(np.cos(ang)), np.abs(np.sin(ang))
+    lo, hi = np.abs(x[..., :h]), np.abs(x[..., h:])
+    e = 2.0 ** -21 * (lo * c + hi * s)
+    e2 = 2.0 ** -21 * (hi * c + lo * s)
+    return np.concatenate([e, e2], axis=-1)
+
+
+def prepare(src_bits, pos, hq: int, hkv: int, d: int, mode: str, q_scale=None, inv_freq=None,
+            with_allowance: bool = False):
     """Prepared q and k of every token (float64, before the final bf16 rounding) and v's bits.
 
     src_bits [n, (hq + 2 hkv) * d] bf16 bits, pos [n].  Returns (q [n, hq, d], k [n, hkv, d],
-    v_bits [n, hkv, d]).  Tokens with a negative position are not written by the step; the
-    oracle still returns their values."""
+    v_bits [n, hkv, d]), and with ``with_allowance`` also the absolute allowances (q_tol, k_tol)
+    of the l2_rope preparation (None for rmsnorm, whose allowance is relative).  Tokens with a
+    negative position are not written by the step; the oracle still returns their values."""
     src = np.asarray(src_bits).astype(np.uint16)
     n = src.shape[0]
     x = bf16_to_f64(src[:, :(hq + 2 * hkv) * d]).reshape(n, hq + 2 * hkv, d)
     xq, xk = x[:, :hq], x[:, hq:hq + hkv]
     v_bits = src[:, (hq + hkv) * d:(hq + 2 * hkv) * d].reshape(n, hkv, d)
     if mode == "rmsnorm":
-        return rmsnorm_head(xq), rmsnorm_head(xk), v_bits
+        out = (rmsnorm_head(xq), rmsnorm_head(xk), v_bits)
+        return out + (None, None) if with_allowance else out
     if mode != "l2_rope":
         raise ValueError(mode)
     qs = np.ones(d) if q_scale is None else np.asarray(q_scale, dtype=np.float32).astype(np.float64)
     q_out = np.empty((n, hq, d))
     k_out = np.empty((n, hkv, d))
+    q_tol = np.empty((n, hq, d))
+    k_tol = np.empty((n, hkv, d))
     for t in range(n):
         ang = rope_angle32(int(pos[t]), inv_freq)
-        rq = _rn(rope_rotate_half(xq[t], ang))           # rounding point: rotated head
-        rk = _rn(rope_rotate_half(xk[t], ang))
+        rq64 = rope_rotate_half(xq[t], ang)
+        rk64 = rope_rotate_half(xk[t], ang)
+        rq = _rn(rq64)                                    # rounding point: rotated head
+        rk = _rn(rk64)
         qn = _rn(l2_head(rq))                             # rounding point: normalised head
         q_out[t] = qs * qn                                # rounded by the check: q after the scale
         k_out[t] = l2_head(rk)                            # rounded by the check
+        if with_allowance:
+            for r64, xh, sc, o, tol in ((rq64, xq[t], qs, q_out[t], q_tol), (rk64, xk[t], 1.0, k_out[t], k_tol)):
+                e = _rotation_bound(xh, ang)
+                norm = np.sqrt(np.sum(_rn(r64) ** 2, axis=-1, keepdims=True) + L2_EPS)
+                tol[t] = REL_L2ROPE * np.abs(o) + sc * (e + _ulp_bf16(np.abs(r64) + e)) / norm
+    if with_allowance:
+        return q_out, k_out, v_bits, q_tol, k_tol
     return q_out, k_out, v_bits
 
 
-def check_prep(gpu_bits, ref, rel: float, min_bit_equal: float = 0.99) -> dict:
-    """bf16 outputs against float64 values with a relative allowance before the final rounding.
+def check_prep(gpu_bits, ref, tol, min_bit_equal: float = 0.99) -> dict:
+    """bf16 outputs against float64 values with an allowance before the final rounding.
 
-    An output passes when it lies in [RN(o - rel |o|), RN(o + rel |o|)] in value order.  On top,
-    the share of outputs equal to RN(o) must reach ``min_bit_equal``: a missing or extra rounding
-    point moves a large share of outputs by one step while staying inside the allowance."""
+    ``tol`` is a relative allowance (a float) or an array of absolute allowances.  An output
+    passes when it lies in [RN(o - t), RN(o + t)] in value order.  On top, the share of outputs
+    equal to RN(o) must reach ``min_bit_equal``: a missing or extra rounding point moves a large
+    share of outputs by one step while staying inside the allowance."""
     from .check import compare
     o = np.asarray(ref, dtype=np.float64)
-    r = compare(gpu_bits, o, rel * np.abs(o).ravel())
+    if np.ndim(tol) == 0:
+        t = float(tol) * np.abs(o).ravel()
+    else:
+        t = np.asarray(tol, dtype=np.float64).ravel()
+    r = compare(gpu_bits, o, t)
     fin = int(np.isfinite(o).sum())
     r["bit_equal_share"] = r["n_bit_equal"] / max(1, fin)
     r["ok"] = bool(r["ok"] and r["bit_equal_share"] >= min_bit_equal)

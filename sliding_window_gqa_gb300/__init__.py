@@ -17,7 +17,7 @@ import re
 import torch
 
 __all__ = [
-    "WAError", "lib", "lib_path", "decode", "prompt", "status", "decode_ws_bytes", "prompt_ws_bytes",
+    "WAError", "lib", "lib_path", "decode", "prompt", "prep_append", "status", "decode_ws_bytes", "prompt_ws_bytes",
     "WA_OK", "WA_EINVAL", "WA_EWORKSPACE", "WA_ECUDA", "WA_EDEVICE",
     "WA_STATUS_BAD_POS", "WA_STATUS_BAD_HI", "WA_STATUS_TIMEOUT",
 ]
@@ -58,6 +58,11 @@ class _Strides(ctypes.Structure):
     _fields_ = [("q", ctypes.c_int64), ("k", ctypes.c_int64), ("v", ctypes.c_int64), ("out", ctypes.c_int64)]
 
 
+class _PrepLayout(ctypes.Structure):
+    _fields_ = [("src_tok", ctypes.c_int64), ("q_tok", ctypes.c_int64), ("ring_row", ctypes.c_int64),
+                ("slot", ctypes.c_int64)]
+
+
 _lib = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
@@ -84,6 +89,9 @@ def lib() -> ctypes.CDLL:
         L.wa_prompt.argtypes = [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, ctypes.c_float, _I,
                                 ctypes.POINTER(_Strides), _P, _P, ctypes.c_size_t, _P]
         L.wa_prompt.restype = ctypes.c_int
+        L.wa_prep_append.argtypes = [_P, _P, _I, _I, _I, _I, _I, _P, _P, _I, ctypes.POINTER(_PrepLayout),
+                                     _P, _P, _P, _P, ctypes.c_size_t, _P]
+        L.wa_prep_append.restype = ctypes.c_int
         L.wa_status.argtypes = [_P, _P]
         L.wa_status.restype = ctypes.c_int
         L.wa_strerror.argtypes = [ctypes.c_int]
@@ -172,6 +180,59 @@ def prompt(q, k, v, p0: int, hi=None, win: int = 0, scale: float = 1.0, p32: boo
     if rc != WA_OK:
         raise WAError(rc, "wa_prompt")
     return out
+
+
+_PREP_MODES = {"rmsnorm": _C["WA_PREP_RMSNORM"], "l2_rope": _C["WA_PREP_L2_ROPE"]}
+
+
+def _ring_layout(name: str, t: torch.Tensor, d: int):
+    """(ring, ring_row, slot) of a [ring, hkv, d] shared ring or [tokens, ring, hkv, d] per-token rings."""
+    if t.stride(-1) != 1 or t.stride(-2) != d:
+        raise ValueError(f"{name} must have head stride d and unit dim stride")
+    if t.dim() == 3:
+        return t.shape[0], 0, int(t.stride(0))
+    if t.dim() == 4:
+        return t.shape[1], int(t.stride(0)), int(t.stride(1))
+    raise ValueError(f"{name} must be [ring, hkv, d] or [tokens, ring, hkv, d]")
+
+
+def prep_append(src, pos, q_out, k_ring, v_ring=None, mode: str = "rmsnorm", q_scale=None, inv_freq=None,
+                ws=None, stream=None):
+    """q/k preparation and KV append.
+
+    src [n, >= (hq + 2 hkv) d] bf16 projection rows (unit inner stride), pos int32 [n],
+    q_out [n, hq, d] (token-strided), k_ring / v_ring [ring, hkv, d] (one shared ring) or
+    [n, ring, hkv, d] (one ring per token).  v_ring None leaves v where it is.  mode "rmsnorm"
+    or "l2_rope" (then inv_freq fp32 [d/2], q_scale fp32 [d] or None).  Returns the workspace,
+    whose status wa_status / status() reads."""
+    _check_bf16("src", src)
+    _check_bf16("q_out", q_out)
+    _check_bf16("k_ring", k_ring)
+    if v_ring is not None:
+        _check_bf16("v_ring", v_ring)
+    if pos.dtype != torch.int32 or not pos.is_cuda:
+        raise TypeError("pos must be an int32 CUDA tensor")
+    if src.dim() != 2 or src.stride(1) != 1:
+        raise ValueError("src must be [n, row] with unit inner stride")
+    n = src.shape[0]
+    d = k_ring.shape[-1]
+    hq, hkv = q_out.shape[1], k_ring.shape[-2]
+    ring, ring_row, slot = _ring_layout("k_ring", k_ring, d)
+    if v_ring is not None and _ring_layout("v_ring", v_ring, d) != (ring, ring_row, slot):
+        raise ValueError("v_ring must have k_ring's layout")
+    for n_, t, cnt in (("q_scale", q_scale, d), ("inv_freq", inv_freq, d // 2)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.numel() != cnt):
+            raise TypeError(f"{n_} must be a contiguous fp32 CUDA tensor of {cnt} elements")
+    lay = _PrepLayout(int(src.stride(0)), _token_stride("q_out", q_out, d), ring_row, slot)
+    ws = _workspace(256, src.device, ws)
+    rc = lib().wa_prep_append(src.data_ptr(), pos.data_ptr(), n, hq, hkv, d, _PREP_MODES[mode],
+                              None if q_scale is None else q_scale.data_ptr(),
+                              None if inv_freq is None else inv_freq.data_ptr(), ring, ctypes.byref(lay),
+                              q_out.data_ptr(), k_ring.data_ptr(), None if v_ring is None else v_ring.data_ptr(),
+                              ws.data_ptr(), ws.numel(), _stream_handle(stream))
+    if rc != WA_OK:
+        raise WAError(rc, "wa_prep_append")
+    return ws
 
 
 def status(ws, stream=None) -> int:

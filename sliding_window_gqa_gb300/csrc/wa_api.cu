@@ -160,6 +160,36 @@ int wa_prompt(const void* q, const void* k, const void* v, int32_t p0, int32_t n
     return WA_OK;
 }
 
+int wa_prep_append(const void* src, const int32_t* pos, int32_t n, int32_t hq, int32_t hkv, int32_t d,
+                   int32_t mode, const float* q_scale, const float* inv_freq, int32_t ring,
+                   const wa_prep_layout* lay, void* q_out, void* k_ring, void* v_ring,
+                   void* ws, size_t ws_bytes, void* stream) {
+    if (!src || !pos || !lay || !q_out || !k_ring) return WA_EINVAL;
+    if (n <= 0 || !heads_ok(hq, hkv) || ring <= 0) return WA_EINVAL;
+    if (d != 128 && d != 256) return WA_EINVAL;
+    if (mode != WA_PREP_RMSNORM && mode != WA_PREP_L2_ROPE) return WA_EINVAL;
+    if (mode == WA_PREP_L2_ROPE && !inv_freq) return WA_EINVAL;
+    if (!aligned16(src) || !aligned16(q_out) || !aligned16(k_ring) || (v_ring && !aligned16(v_ring))) return WA_EINVAL;
+    if (lay->src_tok < (hq + 2 * hkv) * static_cast<int64_t>(d) || lay->q_tok < hq * static_cast<int64_t>(d) ||
+        lay->ring_row < 0 || lay->slot < hkv * static_cast<int64_t>(d))
+        return WA_EINVAL;
+    if ((lay->src_tok | lay->q_tok | lay->ring_row | lay->slot) & 7) return WA_EINVAL;
+    if (!ws || ws_bytes < WA_PREP_WS_BYTES || (reinterpret_cast<uintptr_t>(ws) & 255u)) return WA_EWORKSPACE;
+    const int rc = ensure_device();
+    if (rc != WA_OK) return rc;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    wa::PrepArgs a{};
+    a.src = src; a.pos = pos; a.q_scale = mode == WA_PREP_L2_ROPE ? q_scale : nullptr; a.inv_freq = inv_freq;
+    a.q_out = q_out; a.k_ring = k_ring; a.v_ring = v_ring;
+    a.n = n; a.hq = hq; a.hkv = hkv; a.d = d; a.ring = ring; a.mode = mode;
+    a.src_tok = lay->src_tok; a.q_tok = lay->q_tok; a.ring_row = lay->ring_row; a.slot = lay->slot;
+    a.hdr = static_cast<wa::WsHeader*>(ws);
+    if (cudaMemsetAsync(ws, 0, wa::kHeaderBytes, s) != cudaSuccess) return WA_ECUDA;
+    if (wa::launch_prep(a, s) != cudaSuccess) return WA_ECUDA;
+    return WA_OK;
+}
+
 int wa_status(const void* ws, void* stream) {
     if (!ws) return WA_EWORKSPACE;
     int st = 0;
@@ -177,7 +207,7 @@ const char* wa_strerror(int code) {
         case WA_ECUDA: return "CUDA call or launch failed";
         case WA_EDEVICE: return "device is not compute capability 10.3 (GB300)";
         case WA_ESTATIC: return "sizes need more scratch than wa_decode_static's fixed 16 MiB array";
-        case WA_STATUS_BAD_POS: return "status: a decode position was out of range (clamped)";
+        case WA_STATUS_BAD_POS: return "status: a decode or append position was out of range (clamped or skipped)";
         case WA_STATUS_BAD_HI: return "status: a prompt hi[i] was out of range (clamped)";
         case WA_STATUS_TIMEOUT: return "status: a device wait ran out; outputs are not valid";
         case WA_STATUS_LAYOUT: return "status: shared memory misaligned; outputs were not written";

@@ -66,12 +66,27 @@ struct RerunArgs {
     const int* flags;
 };
 
+// q/k preparation and KV append (mode WA_PREP_*).
+struct PrepArgs {
+    const void* src;
+    const int32_t* pos;
+    const float* q_scale;    // may be null
+    const float* inv_freq;   // WA_PREP_L2_ROPE only
+    void* q_out;
+    void* k_ring;
+    void* v_ring;            // may be null
+    int n, hq, hkv, d, ring, mode;
+    int64_t src_tok, q_tok, ring_row, slot;
+    WsHeader* hdr;
+};
+
 // cuTensorMapEncodeTiled from the driver, looked up once; null if unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_prompt(const PromptArgs& a, cudaStream_t s);
 cudaError_t launch_rerun(const RerunArgs& a, cudaStream_t s);
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t prompt_prepare_device(int dev);
 cudaError_t decode_prepare_device(int dev);
 // Decode partials on the tensor cores (query-head groups of kTcMinGroup and more); the merge is shared.

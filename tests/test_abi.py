@@ -87,6 +87,35 @@ def test_argument_errors_before_any_cuda_call():
     assert pcall(hq=48, hkv=2) == E
 
 
+def test_prep_append_argument_errors_before_any_cuda_call():
+    wa = ensure_built()
+    L = wa.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    E = wa.WA_EINVAL
+    d, hq, hkv = 256, 16, 4
+
+    def call(lay=None, **kw):
+        a = dict(src=fake, pos=fake, n=8, hq=hq, hkv=hkv, d=d, mode=2, qs=None, inv=fake, ring=1536, q=fake, k=fake,
+                 v=fake, ws=fake, ws_bytes=256, stream=None)
+        a.update(kw)
+        lay = lay or wa._PrepLayout((hq + 2 * hkv) * d, hq * d, 1536 * hkv * d, hkv * d)
+        return L.wa_prep_append(a["src"], a["pos"], a["n"], a["hq"], a["hkv"], a["d"], a["mode"], a["qs"], a["inv"],
+                                a["ring"], ctypes.byref(lay), a["q"], a["k"], a["v"], a["ws"], a["ws_bytes"],
+                                a["stream"])
+
+    assert call(src=None) == E
+    assert call(mode=3) == E
+    assert call(inv=None) == E                      # the RoPE needs its frequencies
+    assert call(d=192) == E
+    assert call(hq=12, hkv=8) == E
+    assert call(ring=0) == E
+    assert call(k=ctypes.c_void_p((1 << 20) + 8)) == E
+    assert call(lay=wa._PrepLayout(100, hq * d, 0, hkv * d)) == E             # row shorter than the heads
+    assert call(lay=wa._PrepLayout((hq + 2 * hkv) * d + 4, hq * d, 0, hkv * d)) == E   # not a multiple of 8
+    assert call(ws=None) == wa.WA_EWORKSPACE
+    assert call(ws_bytes=128) == wa.WA_EWORKSPACE
+
+
 def test_strerror_and_version():
     wa = ensure_built()
     L = wa.lib()

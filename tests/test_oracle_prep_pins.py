@@ -141,11 +141,11 @@ def test_checker_rejects_a_dropped_rounding_point(drop):
     pos = rng.integers(0, 200_000, n)
     inv = (1.0 / 10000.0 ** (np.arange(0, d, 2) / d)).astype(np.float32)
     qs = rng.uniform(0.5, 2.0, d).astype(np.float32)
-    q_ref, _, _ = prep.prepare(src, pos, hq, hkv, d, "l2_rope", qs, inv)
+    q_ref, _, _, q_tol, _ = prep.prepare(src, pos, hq, hkv, d, "l2_rope", qs, inv, with_allowance=True)
     good = oracle.f64_to_bf16(_planted_l2_rope(src, pos, hq, hkv, d, qs, inv, drop=None))
-    assert prep.check_prep(good, q_ref, prep.REL_L2ROPE)["ok"]
+    assert prep.check_prep(good, q_ref, q_tol)["ok"]
     bad = oracle.f64_to_bf16(_planted_l2_rope(src, pos, hq, hkv, d, qs, inv, drop=drop))
-    r = prep.check_prep(bad, q_ref, prep.REL_L2ROPE)
+    r = prep.check_prep(bad, q_ref, q_tol)
     assert not r["ok"], r
 
 
@@ -155,12 +155,37 @@ def test_checker_rejects_sign_error_and_swapped_halves():
     src = _src(rng, n, hq, hkv, d)
     pos = rng.integers(1, 50_000, n)
     inv = (1.0 / 10000.0 ** (np.arange(0, d, 2) / d)).astype(np.float32)
-    q_ref, k_ref, _ = prep.prepare(src, pos, hq, hkv, d, "l2_rope", None, inv)
+    q_ref, k_ref, _, _, k_tol = prep.prepare(src, pos, hq, hkv, d, "l2_rope", None, inv, with_allowance=True)
     x = oracle.bf16_to_f64(src).reshape(n, hq + 2 * hkv, d)[:, hq:hq + hkv]
     for t in range(n):
         ang = prep.rope_angle32(int(pos[t]), inv)
         wrong = prep.l2_head(prep._rn(prep.rope_rotate_half(x[t], -ang)))   # rotation the wrong way
-        assert not prep.check_prep(oracle.f64_to_bf16(wrong), k_ref[t], prep.REL_L2ROPE)["ok"]
+        assert not prep.check_prep(oracle.f64_to_bf16(wrong), k_ref[t], k_tol[t])["ok"]
+        halves = np.concatenate([x[t][:, d // 2:], x[t][:, :d // 2]], axis=-1)   # halves swapped
+        wrong = prep.l2_head(prep._rn(prep.rope_rotate_half(halves, ang)))
+        assert not prep.check_prep(oracle.f64_to_bf16(wrong), k_ref[t], k_tol[t])["ok"]
+
+
+def test_rotation_allowance_covers_fp32_cancellation():
+    """An fp32 evaluation of the rotation (numpy float32, correctly rounded cos/sin) stays inside
+    the allowance, including rows where the two terms cancel."""
+    rng = np.random.default_rng(11)
+    n, hq, hkv, d = 64, 4, 2, 128
+    src = _src(rng, n, hq, hkv, d)
+    pos = rng.integers(0, 200_000, n)
+    inv = (1.0 / 10000.0 ** (np.arange(0, d, 2) / d)).astype(np.float32)
+    _, k_ref, _, _, k_tol = prep.prepare(src, pos, hq, hkv, d, "l2_rope", None, inv, with_allowance=True)
+    x = oracle.bf16_to_f64(src).reshape(n, hq + 2 * hkv, d)[:, hq:hq + hkv].astype(np.float32)
+    out = np.empty((n, hkv, d))
+    for t in range(n):
+        ang = prep.rope_angle32(int(pos[t]), inv).astype(np.float32)
+        c, s = np.cos(ang.astype(np.float64)).astype(np.float32), np.sin(ang.astype(np.float64)).astype(np.float32)
+        lo, hi = x[t][:, :d // 2], x[t][:, d // 2:]
+        r = np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1).astype(np.float64)
+        r = prep._rn(r)
+        ss = np.sum((r * r).astype(np.float32), axis=-1, keepdims=True, dtype=np.float32)
+        out[t] = (r.astype(np.float32) * (np.float32(1) / np.sqrt(ss + np.float32(1e-6)))).astype(np.float64)
+    assert prep.check_prep(oracle.f64_to_bf16(out), k_ref, k_tol)["ok"]
 
 
 def test_checker_rmsnorm_allowance_is_tight_enough():
