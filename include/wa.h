@@ -129,6 +129,9 @@ size_t wa_prompt_ws_bytes(int32_t n, int32_t hq);
  *   hi   [n] int32, device, or NULL: row i sees keys [lo_i, hi[i]] with
  *        p0+i <= hi[i] <= p0+n-1; NULL means hi[i] = p0+i (causal)
  *   p32  0: P enters P.V as one bf16; 1: as bf16(P) + bf16(P - bf16(P))
+ *        (bullet "Window.p32"); 2: as three bf16 parts hi + mid + lo whose fp32
+ *        sum is P (TensorFold pull request #1622, review thread), which with
+ *        the exact bf16 q.k products keeps the result to fp32 accuracy
  *   out  [n, hq, d]      bf16, token stride strides->out (default hq*d)
  *
  * Tensor-core tiles (tcgen05, accumulators in tensor memory, operands staged

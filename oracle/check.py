@@ -21,6 +21,9 @@ from . import bf16_to_f64, f64_to_bf16
 TOL_FP32_P = 3e-3
 TOL_P32 = 3e-3
 TOL_BF16_P = 8e-3
+# P in three bf16 parts: the fp32-accurate mode, held to the scalar kernel's bound 1e-5
+# (TensorFold pull request #1622, review thread: "holds the tile to 1e-5 against fp64")
+TOL_P3 = 1e-5
 
 
 def order_key(bits) -> np.ndarray:

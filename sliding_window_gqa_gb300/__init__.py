@@ -156,12 +156,13 @@ def _token_stride(name: str, t: torch.Tensor, d: int) -> int:
     return int(t.stride(0))
 
 
-def prompt(q, k, v, p0: int, hi=None, win: int = 0, scale: float = 1.0, p32: bool = False,
+def prompt(q, k, v, p0: int, hi=None, win: int = 0, scale: float = 1.0, p32=False,
            out=None, ws=None, stream=None):
     """Prompt attention for rows p0 .. p0+n-1: q [n,hq,d], k/v [ring,hkv,d] (bf16, token-strided).
 
     ``hi`` is None (each row's last key is its own position) or an int32 CUDA
-    tensor [n].  Returns out [n,hq,d] bf16."""
+    tensor [n].  ``p32``: False / 0 (one bf16 P), True / 1 (two parts) or 2 (three
+    parts).  Returns out [n,hq,d] bf16."""
     for n_, t in (("q", q), ("k", k), ("v", v)):
         _check_bf16(n_, t)
     n, hq, d = q.shape
@@ -175,7 +176,7 @@ def prompt(q, k, v, p0: int, hi=None, win: int = 0, scale: float = 1.0, p32: boo
     ws = _workspace(prompt_ws_bytes(n, hq), q.device, ws)
     rc = lib().wa_prompt(q.data_ptr(), k.data_ptr(), v.data_ptr(), int(p0), n,
                          None if hi is None else hi.data_ptr(), hq, hkv, d, int(win), ring, float(scale),
-                         1 if p32 else 0, ctypes.byref(st), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                         int(p32), ctypes.byref(st), out.data_ptr(), ws.data_ptr(), ws.numel(),
                          _stream_handle(stream))
     if rc != WA_OK:
         raise WAError(rc, "wa_prompt")

@@ -111,7 +111,7 @@ int wa_prompt(const void* q, const void* k, const void* v, int32_t p0, int32_t n
     if (n <= 0 || p0 < 0 || !heads_ok(hq, hkv) || hq > 65535) return WA_EINVAL;
     if (d != 128 && d != 256) return WA_EINVAL;
     if (win < 0 || ring <= 0 || win > ring) return WA_EINVAL;
-    if (p32 != 0 && p32 != 1) return WA_EINVAL;
+    if (p32 < 0 || p32 > 2) return WA_EINVAL;
     if (!std::isfinite(scale)) return WA_EINVAL;
     if (static_cast<int64_t>(p0) + n > INT32_MAX) return WA_EINVAL;
     if (win > 0) {

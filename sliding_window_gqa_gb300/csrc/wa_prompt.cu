@@ -6,7 +6,13 @@
 // not depend on how the prompt is chunked), "Window.p32" (P enters P.V as
 // bf16(P) + bf16(P - bf16(P))), "promptRows(..., hi)" (row i sees keys
 // [p0 + i - win + 1, hi[i]]) and "Scale is a parameter" (window 0 = linear
-// cache).  Probabilities are fp32; the running softmax is fp32.
+// cache).  Probabilities are fp32; the running softmax is fp32.  A third
+// P mode carries P as three bf16 parts (hi, mid, lo) whose fp32 sum is P, one
+// P.V product per part (TensorFold pull request #1622, review thread: q*scale
+// and P "each carried as three 16-bit parts ... with one matrix op per part").
+// Here q enters S unscaled and exact, and the scale is applied to S in fp32,
+// so only P needs the split; S and the three-part P.V are then accurate to
+// fp32.
 //
 // GB300 design (one CTA per 128-row query tile of one query head):
 //   warp 0      TMA producer: Q once, then K and V tiles of T keys into two
@@ -53,9 +59,10 @@ struct PromptParams {
     int neg;          // scale < 0: the S MMA negates Q
 };
 
-template <int D, bool P32>
+// NP: the parts P enters P.V as (1: bf16(P); 2: hi, lo; 3: hi, mid, lo).
+template <int D, int NP>
 struct Cfg {
-    static constexpr int T = (D == 256) ? 64 : 128;   // keys per tile
+    static constexpr int T = (D == 256 || NP == 3) ? 64 : 128;   // keys per tile
     static constexpr int NC = T / 2;                  // S columns per softmax thread
     static constexpr int KB = D / 64;                 // 64-element (128-byte) column blocks
     static constexpr int Q_BLOCK = kBM * 128;
@@ -66,8 +73,9 @@ struct Cfg {
     static constexpr int OFF_K = OFF_Q + Q_BYTES;               // 2 stages
     static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;          // 2 stages
     // P lives in tensor memory (the A operand of P.V): two buffers (tiles alternate) for a
-    // single bf16 P, one buffer of two halves (hi, lo) for P32; T / 2 columns each.
-    static constexpr int P_BUFS = P32 ? 1 : 2;
+    // single bf16 P, one buffer of NP parts otherwise; T / 2 columns each.
+    static constexpr int P_BUFS = NP == 1 ? 2 : 1;
+    static constexpr int P_SLOTS = NP == 1 ? 2 : NP;
     static constexpr int OFF_X = OFF_V + 2 * KV_BYTES;          // row exchange [2 tiles][2 halves][128] fp32
     static constexpr int OFF_BAR = OFF_X + 2 * 2 * kBM * 4;
     static constexpr int NBAR = 24;
@@ -76,9 +84,9 @@ struct Cfg {
     static constexpr int TMEM_COLS = 512;
     static constexpr int O_COL = 0;
     static constexpr int S_COL = D;                             // S buffers at D and D + T
-    static constexpr int P_COL = D + 2 * T;                     // P: 2 x T/2 columns
-    __host__ __device__ static constexpr int p_col(int buf_or_half) { return P_COL + buf_or_half * (T / 2); }
-    static_assert(D + 3 * T <= TMEM_COLS, "tensor memory budget");
+    static constexpr int P_COL = D + 2 * T;                     // P: P_SLOTS x T/2 columns
+    __host__ __device__ static constexpr int p_col(int buf_or_part) { return P_COL + buf_or_part * (T / 2); }
+    static_assert(P_COL + P_SLOTS * (T / 2) <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -168,9 +176,9 @@ __device__ __forceinline__ void load_s(uint32_t taddr, float (&sv)[NC]) {
     }
 }
 
-template <int D, bool P32>
+template <int D, int NP>
 __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_constant__ PromptParams p) {
-    using C = Cfg<D, P32>;
+    using C = Cfg<D, NP>;
     constexpr int T = C::T;
     constexpr int NC = C::NC;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -341,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
                     tc_fence_after();
                     const uint32_t vst = sbase + C::OFF_V + ps * C::KV_BYTES;
 #pragma unroll
-                    for (int half = 0; half < (P32 ? 2 : 1); ++half) {
-                        const uint32_t pt = tbase + C::p_col(P32 ? half : (pidx & 1));
+                    for (int half = 0; half < NP; ++half) {
+                        const uint32_t pt = tbase + C::p_col(NP > 1 ? half : (pidx & 1));
 #pragma unroll
                         for (int kk = 0; kk < T / 16; ++kk) {
                             const uint64_t b = sdesc_sw128(vst + kk * 16 * 128, C::KV_BLOCK, 1024);
@@ -476,25 +484,25 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
                     tmem_wait_st();
                 }
             }
-            // P (and its residual for P32) into tensor memory, two bf16 per column, this thread's columns
+            // P (and its residual parts) into tensor memory, two bf16 per column, this thread's
+            // columns.  Each residual p - part is exact in fp32.
             {
-                uint32_t w[NC / 2], wl[NC / 2];
+                uint32_t w[NP][NC / 2];
 #pragma unroll
                 for (int e = 0; e < NC / 2; ++e) {
-                    const float a = sv[2 * e], b = sv[2 * e + 1];
-                    w[e] = pack_bf16(a, b);
-                    if constexpr (P32) {
-                        const float ah = __uint_as_float(w[e] << 16), bh = __uint_as_float(w[e] & 0xFFFF0000u);
-                        wl[e] = pack_bf16(a - ah, b - bh);
+                    float a = sv[2 * e], b = sv[2 * e + 1];
+#pragma unroll
+                    for (int part = 0; part < NP; ++part) {
+                        w[part][e] = pack_bf16(a, b);
+                        a -= __uint_as_float(w[part][e] << 16);
+                        b -= __uint_as_float(w[part][e] & 0xFFFF0000u);
                     }
                 }
-                const uint32_t pa = tbase + lane_addr + C::p_col(P32 ? 0 : (idx & 1)) + col0 / 2;
-                if constexpr (NC == 64) {
-                    tmem_st32(pa, w);
-                    if constexpr (P32) tmem_st32(tbase + lane_addr + C::p_col(1) + col0 / 2, wl);
-                } else {
-                    tmem_st16(pa, w);
-                    if constexpr (P32) tmem_st16(tbase + lane_addr + C::p_col(1) + col0 / 2, wl);
+#pragma unroll
+                for (int part = 0; part < NP; ++part) {
+                    const uint32_t pa = tbase + lane_addr + C::p_col(NP > 1 ? part : (idx & 1)) + col0 / 2;
+                    if constexpr (NC == 64) tmem_st32(pa, w[part]);
+                    else tmem_st16(pa, w[part]);
                 }
                 tmem_wait_st();
             }
@@ -570,9 +578,9 @@ bool encode_3d(CUtensorMap* m, const void* base, int d, int heads, int tokens, i
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool P32>
+template <int D, int NP>
 cudaError_t launch_t(const PromptArgs& a, cudaStream_t s) {
-    using C = Cfg<D, P32>;
+    using C = Cfg<D, NP>;
     PromptParams pp{};
     if (!encode_3d(&pp.tq, a.q, D, a.hq, a.n, a.q_tok, kBM) || !encode_3d(&pp.tk, a.k, D, a.hkv, a.ring, a.k_tok, C::T) ||
         !encode_3d(&pp.tv, a.v, D, a.hkv, a.ring, a.v_tok, C::T))
@@ -592,13 +600,13 @@ cudaError_t launch_t(const PromptArgs& a, cudaStream_t s) {
     pp.neg = a.scale < 0.f ? 1 : 0;
     pp.c = (a.scale < 0.f ? -a.scale : a.scale) * 1.4426950408889634f;
     const dim3 grid(pp.nqt, a.hq);
-    prompt_kernel<D, P32><<<grid, kThreads, C::SMEM, s>>>(pp);
+    prompt_kernel<D, NP><<<grid, kThreads, C::SMEM, s>>>(pp);
     return cudaGetLastError();
 }
 
-template <int D, bool P32>
+template <int D, int NP>
 cudaError_t set_attr() {
-    return cudaFuncSetAttribute(prompt_kernel<D, P32>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, P32>::SMEM);
+    return cudaFuncSetAttribute(prompt_kernel<D, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, NP>::SMEM);
 }
 
 }  // namespace
@@ -619,16 +627,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 cudaError_t prompt_prepare_device(int) {
     cudaError_t e;
     if ((e = get_encoder()) != cudaSuccess) return e;
-    if ((e = set_attr<128, false>()) != cudaSuccess) return e;
-    if ((e = set_attr<128, true>()) != cudaSuccess) return e;
-    if ((e = set_attr<256, false>()) != cudaSuccess) return e;
-    return set_attr<256, true>();
+    if ((e = set_attr<128, 1>()) != cudaSuccess) return e;
+    if ((e = set_attr<128, 2>()) != cudaSuccess) return e;
+    if ((e = set_attr<128, 3>()) != cudaSuccess) return e;
+    if ((e = set_attr<256, 1>()) != cudaSuccess) return e;
+    if ((e = set_attr<256, 2>()) != cudaSuccess) return e;
+    return set_attr<256, 3>();
 }
 
 cudaError_t launch_prompt(const PromptArgs& a, cudaStream_t s) {
     if (get_encoder() != cudaSuccess) return cudaErrorNotSupported;
-    if (a.d == 256) return a.p32 ? launch_t<256, true>(a, s) : launch_t<256, false>(a, s);
-    return a.p32 ? launch_t<128, true>(a, s) : launch_t<128, false>(a, s);
+    if (a.d == 256) {
+        if (a.p32 == 2) return launch_t<256, 3>(a, s);
+        return a.p32 ? launch_t<256, 2>(a, s) : launch_t<256, 1>(a, s);
+    }
+    if (a.p32 == 2) return launch_t<128, 3>(a, s);
+    return a.p32 ? launch_t<128, 2>(a, s) : launch_t<128, 1>(a, s);
 }
 
 }  // namespace wa

@@ -83,7 +83,8 @@ def test_argument_errors_before_any_cuda_call():
     assert pcall(p0=-1) == E
     assert pcall(n=514) == E                  # 514 + 1023 keys do not fit a ring of 1536
     assert pcall(win=0, ring=1000) == E       # linear cache shorter than p0 + n
-    assert pcall(p32=2) == E
+    assert pcall(p32=3) == E
+    assert pcall(p32=-1) == E
     assert pcall(hq=48, hkv=2) == E
 
 

@@ -344,6 +344,24 @@ def test_p32_split_within_2_to_minus_16():
         assert np.all(np.abs(p - (hi + lo)) <= 2.0 ** -16 * p)
 
 
+def test_three_part_split_is_exact_to_fp32():
+    # TensorFold #1622, review thread: P carried as hi + mid + lo 16-bit parts whose fp32 sum
+    # is the value.  Each residual is exact in fp32, and the three parts hold P to 2^-24.
+    rng = np.random.default_rng(6)
+    for e in np.arange(-30, 1):
+        mant = np.concatenate([np.arange(0, 1 << 23, 89, dtype=np.uint32), rng.integers(0, 1 << 23, 4000).astype(np.uint32)])
+        p = ((np.uint32(e + 127) << np.uint32(23)) | mant).view(np.float32).astype(np.float64)
+        p = p[p <= 1.0]
+        parts, r = [], p.copy()
+        for _ in range(3):
+            b16 = oracle.bf16_to_f64(oracle.f64_to_bf16(r))
+            parts.append(b16)
+            nr = r - b16
+            assert np.array_equal(np.float32(nr).astype(np.float64), nr)   # exact in fp32
+            r = nr
+        assert np.all(np.abs(p - (parts[0] + parts[1] + parts[2])) <= 2.0 ** -24 * p)
+
+
 # ---------------------------------------------------------------------------
 # The checker
 # ---------------------------------------------------------------------------

@@ -33,6 +33,8 @@ def wa():
 
 
 def tol(p32):
+    if p32 == 2:
+        return check.TOL_P3
     return check.TOL_P32 if p32 else check.TOL_BF16_P
 
 
@@ -79,6 +81,61 @@ def test_prompt_parity(wa, case):
     assert wa.status(ws) == 0
     r = assert_parity(out, _ref(c), tol(p32), name)
     assert r["n_nonfinite_ref"] == 0
+
+
+P3_CASES = [c[:-1] + (2,) for c in CASES if c[0] in (
+    "chunk512_p1300_image_p32", "wrap333_p5000_bf16", "linear_causal_700_p32", "ring1000_wrapcopy_d128",
+    "d128_sliding_mha", "d128_gqa8_p32", "d256_gqa3", "window_1", "one_row")]
+
+
+@pytest.mark.parametrize("case", P3_CASES, ids=[c[0] + "_as_p3" for c in P3_CASES])
+def test_prompt_parity_three_part_p(wa, case):
+    """P as hi + mid + lo: every output within [RN(o - 1e-5), RN(o + 1e-5)]."""
+    name, n, p0, hq, hkv, d, win, ring, spans, p32 = case
+    c = _case(n, p0, hq, hkv, d, win, ring, seed=zlib.crc32(name.encode()) % 100000, spans=spans)
+    ws = torch.empty(wa.prompt_ws_bytes(n, hq), dtype=torch.uint8, device="cuda")
+    out = wa.prompt(c["q"], c["k"], c["v"], p0, c["hi"], win, 1.0, p32=2, ws=ws)
+    assert wa.status(ws) == 0
+    assert_parity(out, _ref(c), check.TOL_P3, name + " as p3")
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_three_part_p_is_closer_to_float64_than_two_part(wa, d):
+    """Outputs that differ from RN(o): fewer with three parts than with two, and under 0.5 %."""
+    c = _case(700, 0, 16, 8, d, 0, 700, seed=17, outside="keep", peak_every=64)
+    ref = _ref(c)
+    rn = oracle.f64_to_bf16(ref)
+    miss = {}
+    for p32 in (1, 2):
+        out = wa.prompt(c["q"], c["k"], c["v"], 0, None, 0, 1.0, p32=p32)
+        miss[p32] = int((bits(out) != rn.reshape(bits(out).shape)).sum())
+    assert miss[2] < miss[1], miss
+    assert miss[2] < 0.005 * rn.size, miss
+
+
+def test_three_part_p_long_rows_sampled(wa):
+    """Causal 8,192 rows at d 256 and dense 4,096 rows at d 128: sampled rows within 1e-5."""
+    c = _case(8192, 0, 16, 8, 256, 0, 8192, seed=18, outside="keep")
+    out = wa.prompt(c["q"], c["k"], c["v"], 0, None, 0, 1.0, p32=2)
+    rows = [0, 1, 4095, 8190, 8191]
+    assert_parity(out[rows], _ref(c, rows=rows), check.TOL_P3, "causal 8192 p3")
+    dc = wa_synth.dense_qkv_case(4096, 8, 128, seed=19, device="cuda")
+    hi = torch.full((4096,), 4095, dtype=torch.int32, device="cuda")
+    out = wa.prompt(dc["q"], dc["k"], dc["v"], 0, hi, 0, dc["scale"], p32=2)
+    rows = [0, 2048, 4095]
+    ref = oracle.prompt(bits(dc["q"]), bits(dc["k"]), bits(dc["v"]), 0, 0, 4096, dc["scale"],
+                        hi=np.full(4096, 4095), rows=rows)
+    assert_parity(out[rows], ref, check.TOL_P3, "dense 4096 p3")
+
+
+def test_three_part_p_chunk_split_gives_every_rows_bits(wa):
+    n, p0 = 512, 1300
+    c = _case(n, p0, 16, 8, 128, 1024, 1536, seed=20, spans=[(40, 300)], outside="keep")
+    whole = wa.prompt(c["q"], c["k"], c["v"], p0, c["hi"], 1024, 1.0, p32=2)
+    for cut in (1, 301, 384):
+        a = wa.prompt(c["q"][:cut], c["k"], c["v"], p0, c["hi"][:cut].contiguous(), 1024, 1.0, p32=2)
+        b = wa.prompt(c["q"][cut:], c["k"], c["v"], p0 + cut, c["hi"][cut:].contiguous(), 1024, 1.0, p32=2)
+        assert torch.equal(torch.cat([a, b]).view(torch.int16), whole.view(torch.int16)), cut
 
 
 @pytest.mark.parametrize("scale", [0.37, -0.5, 0.0])
