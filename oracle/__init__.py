@@ -47,6 +47,8 @@ __all__ = [
     "attend",
     "decode",
     "prompt",
+    "prompt_sparse",
+    "SPARSE_BLOCK",
 ]
 
 
@@ -200,4 +202,54 @@ def prompt(q, k, v, p0: int, win: int, ring: int, scale: float, hi=None, rows=No
             qq = bf16_to_f64(q[np.ix_(idx, hs)]).reshape(len(idx) * len(hs), d)
             o, _ = attend(qq, kv_k, kv_v, scale)
             out[np.ix_(ris, hs)] = o.reshape(len(idx), len(hs), d)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Block-sparse prompt (TensorFold pull request #1622, "What this changes")
+# ---------------------------------------------------------------------------
+
+SPARSE_BLOCK = 64   # keys per selectable block: positions [64 b, 64 b + 63]
+
+
+def sparse_keys(lo: int, hi: int, sel_row) -> np.ndarray:
+    """Visible keys of a row under a block selection: j in [lo, hi] whose block j // 64 is
+    listed (entries < 0 are unused; repeats and order do not matter), ascending."""
+    blocks = sorted({int(b) for b in np.asarray(sel_row).ravel() if int(b) >= 0})
+    keys = []
+    for b in blocks:
+        a = max(lo, b * SPARSE_BLOCK)
+        e = min(hi, b * SPARSE_BLOCK + SPARSE_BLOCK - 1)
+        if a <= e:
+            keys.extend(range(a, e + 1))
+    return np.asarray(keys, dtype=np.int64)
+
+
+def prompt_sparse(q, k, v, p0: int, win: int, ring: int, scale: float, sel, hi=None, rows=None,
+                  heads=None) -> np.ndarray:
+    """Block-sparse prompt: row i, query head h (key head g = h // G) attends to the keys of
+    [lo_i, hi_i] that lie in the blocks sel[i, g, :] lists ("per-row block masks and causal
+    ends").  q [n,hq,d], k/v [ring,hkv,d] bf16 bits, sel [n, hkv, nsel] int.
+
+    A row with no visible key gets 0 / 0 = NaN (the empty sums of the formula).  Returns float64
+    [len(rows), hq, d]."""
+    q = np.asarray(q); k = np.asarray(k); v = np.asarray(v); sel = np.asarray(sel)
+    n, hq, d = q.shape
+    hkv = k.shape[1]
+    G = hq // hkv
+    rows = list(range(n)) if rows is None else [int(r) for r in rows]
+    heads = list(range(hq)) if heads is None else [int(h) for h in heads]
+    out = np.full((len(rows), hq, d), np.nan)
+    for ri, i in enumerate(rows):
+        lo, hi_i = visible_prompt(p0, i, win, None if hi is None else hi[i])
+        for g in sorted({h // G for h in heads}):
+            hs = [h for h in heads if h // G == g]
+            keys = sparse_keys(lo, hi_i, sel[i, g])
+            if keys.size == 0:
+                continue   # stays NaN
+            slots = keys % ring
+            kv_k = bf16_to_f64(k[slots, g, :])
+            kv_v = bf16_to_f64(v[slots, g, :])
+            o, _ = attend(bf16_to_f64(q[i, hs, :]), kv_k, kv_v, scale)
+            out[ri, hs, :] = o
     return out

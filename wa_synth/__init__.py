@@ -32,6 +32,7 @@ __all__ = [
     "decode_case",
     "prompt_case",
     "dense_qkv_case",
+    "sparse_selection",
     "window_lo",
 ]
 
@@ -189,3 +190,43 @@ def dense_qkv_case(N, H, d, seed, device="cpu", eps=1e-5):
     v = qkv.as_strided((N, H, d), (W, d, 1), 2 * H * d)
     return {"qkv": qkv, "q": q, "k": k, "v": v, "N": N, "H": H, "d": d,
             "scale": 1.0 / math.sqrt(d)}
+
+
+def sparse_selection(n, p0, hkv, nsel, seed, win=0, slice_rows=64, block=64, device="cpu"):
+    """Per-row selected key blocks [n, hkv, nsel] int32 (-1 = unused), shaped like the pages'
+    sparse prompt (TensorFold pull request #1622: 2,048 selected keys a row as 64-key blocks,
+    rows grouped in 64-row slices).
+
+    Row i at position p (block bp = p // block) and key head g select bp and bp - 1 (the
+    causal end), block 0, and a set of random earlier blocks shared by the row's 64-row slice
+    and key head (an indexer's choices are alike for neighbouring rows), up to nsel blocks.
+    Rows whose window holds at most nsel blocks select all of them.  Blocks are drawn from the
+    row's window [window_lo(p), p]."""
+    gen = torch.Generator().manual_seed(int(seed) * 7919 + 17)
+    sel = torch.full((n, hkv, nsel), -1, dtype=torch.int32)
+    shared = {}
+    for i in range(n):
+        p = p0 + i
+        lo_b = window_lo(p, win) // block
+        bp = p // block
+        s = i // slice_rows
+        for g in range(hkv):
+            if bp - lo_b + 1 <= nsel:
+                blocks = list(range(lo_b, bp + 1))
+            else:
+                key = (s, g)
+                if key not in shared:
+                    # candidates: the slice's first row's window minus its own two end blocks
+                    p_first = p0 + s * slice_rows
+                    c_lo = max(window_lo(p_first, win) // block, lo_b, 1)
+                    c_hi = max(c_lo, p_first // block - 2)
+                    perm = torch.randperm(c_hi - c_lo + 1, generator=gen)[:nsel] + c_lo
+                    shared[key] = perm.tolist()
+                blocks = [bp, bp - 1] + ([0] if lo_b == 0 else [])
+                for b in shared[key]:
+                    if len(blocks) >= nsel:
+                        break
+                    if lo_b <= b <= bp and b not in blocks:
+                        blocks.append(b)
+            sel[i, g, :len(blocks)] = torch.tensor(blocks[:nsel], dtype=torch.int32)
+    return sel.to(device)
