@@ -146,6 +146,31 @@ int wa_prompt(const void* q, const void* k, const void* v, int32_t p0, int32_t n
               float scale, int32_t p32, const wa_strides* strides, void* out,
               void* ws, size_t ws_bytes, void* stream);
 
+/* Block-sparse prompt: keys per selectable block, and blocks a row may list. */
+#define WA_SPARSE_BLOCK 64
+#define WA_SPARSE_MAX_SEL 64
+
+/*
+ * Block-sparse prompt form (TensorFold pull request #1622, "What this
+ * changes": per-row block masks and causal ends over selected key blocks).
+ * As wa_prompt, except that row i and query head h (key head g = h / G) see
+ * only the keys of [lo_i, hi[i]] whose block j / WA_SPARSE_BLOCK is listed in
+ * sel[i, g, 0 .. nsel).  Entries < 0 are unused; repeats and order do not
+ * matter.  A row that sees no key gets 0/0 = NaN.
+ *
+ *   sel   [n, hkv, nsel] int32, device; 1 <= nsel <= WA_SPARSE_MAX_SEL
+ *
+ * Each CTA takes one key head, its G query heads and 128 / G rows, and runs
+ * over the union of those rows' visible selected blocks in key order; a block
+ * a row did not select adds nothing to that row, so its bits do not depend on
+ * the other rows.  The key span [max(0, p0 - win + 1), p0 + n - 1] may cover
+ * at most 65,536 blocks.  Returns WA_EINVAL otherwise, or if sel is NULL.
+ */
+int wa_prompt_sparse(const void* q, const void* k, const void* v, int32_t p0, int32_t n,
+                     const int32_t* hi, int32_t hq, int32_t hkv, int32_t d, int32_t win, int32_t ring,
+                     float scale, int32_t p32, const int32_t* sel, int32_t nsel, const wa_strides* strides,
+                     void* out, void* ws, size_t ws_bytes, void* stream);
+
 /* Preparations for wa_prep_append. */
 #define WA_PREP_RMSNORM 1     /* per-head RMSNorm of q and k */
 #define WA_PREP_L2_ROPE 2     /* rotate-half RoPE, L2 norm, q scale */

@@ -17,7 +17,7 @@ import re
 import torch
 
 __all__ = [
-    "WAError", "lib", "lib_path", "decode", "prompt", "prep_append", "status", "decode_ws_bytes", "prompt_ws_bytes",
+    "WAError", "lib", "lib_path", "decode", "prompt", "prompt_sparse", "prep_append", "status", "decode_ws_bytes", "prompt_ws_bytes",
     "WA_OK", "WA_EINVAL", "WA_EWORKSPACE", "WA_ECUDA", "WA_EDEVICE",
     "WA_STATUS_BAD_POS", "WA_STATUS_BAD_HI", "WA_STATUS_TIMEOUT",
 ]
@@ -89,6 +89,9 @@ def lib() -> ctypes.CDLL:
         L.wa_prompt.argtypes = [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, ctypes.c_float, _I,
                                 ctypes.POINTER(_Strides), _P, _P, ctypes.c_size_t, _P]
         L.wa_prompt.restype = ctypes.c_int
+        L.wa_prompt_sparse.argtypes = [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P, _I,
+                                       ctypes.POINTER(_Strides), _P, _P, ctypes.c_size_t, _P]
+        L.wa_prompt_sparse.restype = ctypes.c_int
         L.wa_prep_append.argtypes = [_P, _P, _I, _I, _I, _I, _I, _P, _P, _I, ctypes.POINTER(_PrepLayout),
                                      _P, _P, _P, _P, ctypes.c_size_t, _P]
         L.wa_prep_append.restype = ctypes.c_int
@@ -180,6 +183,33 @@ def prompt(q, k, v, p0: int, hi=None, win: int = 0, scale: float = 1.0, p32=Fals
                          _stream_handle(stream))
     if rc != WA_OK:
         raise WAError(rc, "wa_prompt")
+    return out
+
+
+def prompt_sparse(q, k, v, p0: int, sel, hi=None, win: int = 0, scale: float = 1.0, p32=False,
+                  out=None, ws=None, stream=None):
+    """Block-sparse prompt: as prompt(), with sel an int32 CUDA tensor [n, hkv, nsel] of selected
+    64-key blocks (-1 = unused).  Returns out [n,hq,d] bf16."""
+    for n_, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16(n_, t)
+    n, hq, d = q.shape
+    ring, hkv, _ = k.shape
+    if hi is not None and (hi.dtype != torch.int32 or not hi.is_cuda or hi.numel() != n):
+        raise TypeError("hi must be None or an int32 CUDA tensor of n elements")
+    if sel.dtype != torch.int32 or not sel.is_cuda or not sel.is_contiguous() or sel.dim() != 3 or \
+            sel.shape[0] != n or sel.shape[1] != hkv:
+        raise TypeError("sel must be a contiguous int32 CUDA tensor [n, hkv, nsel]")
+    if out is None:
+        out = torch.empty((n, hq, d), dtype=torch.bfloat16, device=q.device)
+    st = _Strides(_token_stride("q", q, d), _token_stride("k", k, d), _token_stride("v", v, d),
+                  _token_stride("out", out, d))
+    ws = _workspace(prompt_ws_bytes(n, hq), q.device, ws)
+    rc = lib().wa_prompt_sparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), int(p0), n,
+                                None if hi is None else hi.data_ptr(), hq, hkv, d, int(win), ring, float(scale),
+                                int(p32), sel.data_ptr(), sel.shape[2], ctypes.byref(st), out.data_ptr(),
+                                ws.data_ptr(), ws.numel(), _stream_handle(stream))
+    if rc != WA_OK:
+        raise WAError(rc, "wa_prompt_sparse")
     return out
 
 

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libwa.so")
-SOURCES = ["wa_api.cu", "wa_decode.cu", "wa_prompt.cu", "wa_rerun.cu", "wa_static.cu", "wa_decode_tc.cu", "wa_prep.cu"]
+SOURCES = ["wa_api.cu", "wa_decode.cu", "wa_prompt.cu", "wa_rerun.cu", "wa_static.cu", "wa_decode_tc.cu", "wa_prep.cu", "wa_prompt_sparse.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

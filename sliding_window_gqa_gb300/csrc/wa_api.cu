@@ -43,7 +43,8 @@ int ensure_device() {
         g_ready[dev] = WA_EDEVICE;
         return WA_EDEVICE;
     }
-    if (wa::decode_prepare_device(dev) != cudaSuccess || wa::prompt_prepare_device(dev) != cudaSuccess)
+    if (wa::decode_prepare_device(dev) != cudaSuccess || wa::prompt_prepare_device(dev) != cudaSuccess ||
+        wa::prompt_sparse_prepare_device(dev) != cudaSuccess)
         return WA_ECUDA;
     g_ready[dev] = 1;
     return WA_OK;
@@ -103,10 +104,14 @@ size_t wa_prompt_ws_bytes(int32_t n, int32_t hq) {
     return wa::kHeaderBytes + flags_bytes(static_cast<int64_t>(n) * hq);
 }
 
-int wa_prompt(const void* q, const void* k, const void* v, int32_t p0, int32_t n,
-              const int32_t* hi, int32_t hq, int32_t hkv, int32_t d, int32_t win, int32_t ring,
-              float scale, int32_t p32, const wa_strides* strides, void* out,
-              void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// wa_prompt and wa_prompt_sparse: shared checks, workspace carving, launch and re-run.
+int prompt_call(const void* q, const void* k, const void* v, int32_t p0, int32_t n, const int32_t* hi, int32_t hq,
+                int32_t hkv, int32_t d, int32_t win, int32_t ring, float scale, int32_t p32, const int32_t* sel,
+                int32_t nsel, const wa_strides* strides, void* out, void* ws, size_t ws_bytes, void* stream) {
     if (!q || !k || !v || !out) return WA_EINVAL;
     if (n <= 0 || p0 < 0 || !heads_ok(hq, hkv) || hq > 65535) return WA_EINVAL;
     if (d != 128 && d != 256) return WA_EINVAL;
@@ -114,11 +119,17 @@ int wa_prompt(const void* q, const void* k, const void* v, int32_t p0, int32_t n
     if (p32 < 0 || p32 > 2) return WA_EINVAL;
     if (!std::isfinite(scale)) return WA_EINVAL;
     if (static_cast<int64_t>(p0) + n > INT32_MAX) return WA_EINVAL;
+    const int64_t span_lo = win > 0 && p0 - win + 1 > 0 ? p0 - win + 1 : 0;
     if (win > 0) {
-        const int64_t span_lo = p0 - win + 1 > 0 ? p0 - win + 1 : 0;
         if (static_cast<int64_t>(p0) + n - 1 - span_lo >= ring) return WA_EINVAL;
     } else if (static_cast<int64_t>(p0) + n > ring) {
         return WA_EINVAL;
+    }
+    if (sel) {
+        if (nsel < 1 || nsel > WA_SPARSE_MAX_SEL) return WA_EINVAL;
+        // the kernel's union bitmap covers at most 65,536 blocks of the key span
+        if ((static_cast<int64_t>(p0) + n - 1) / WA_SPARSE_BLOCK - span_lo / WA_SPARSE_BLOCK + 1 > 65536)
+            return WA_EINVAL;
     }
     int64_t qs = static_cast<int64_t>(hq) * d, ks = static_cast<int64_t>(hkv) * d, vs = ks, os = qs;
     if (strides) {
@@ -146,18 +157,42 @@ int wa_prompt(const void* q, const void* k, const void* v, int32_t p0, int32_t n
     a.out = out;
     a.hdr = reinterpret_cast<wa::WsHeader*>(base);
     a.flags = reinterpret_cast<int*>(base + wa::kHeaderBytes);
+    a.sel = sel;
+    a.nsel = sel ? nsel : 0;
     if (cudaMemsetAsync(base, 0, wa::kHeaderBytes, s) != cudaSuccess) return WA_ECUDA;
-    const cudaError_t e = wa::launch_prompt(a, s);
+    const cudaError_t e = sel ? wa::launch_prompt_sparse(a, s) : wa::launch_prompt(a, s);
     if (e == cudaErrorNotSupported) return WA_EINVAL;
     if (e != cudaSuccess) return WA_ECUDA;
 
     wa::RerunArgs r{};
-    r.mode = 1; r.q = q; r.k = k; r.v = v; r.idx = hi;
+    r.mode = sel ? 2 : 1; r.q = q; r.k = k; r.v = v; r.idx = hi;
+    r.sel = sel; r.nsel = a.nsel;
     r.rows = n; r.hq = hq; r.hkv = hkv; r.d = d; r.win = win; r.ring = ring; r.p0 = p0; r.scale = scale;
     r.q_tok = qs; r.k_tok = ks; r.v_tok = vs; r.o_tok = os;
     r.out = out; r.hdr = a.hdr; r.flags = a.flags;
     if (wa::launch_rerun(r, s) != cudaSuccess) return WA_ECUDA;
     return WA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wa_prompt(const void* q, const void* k, const void* v, int32_t p0, int32_t n,
+              const int32_t* hi, int32_t hq, int32_t hkv, int32_t d, int32_t win, int32_t ring,
+              float scale, int32_t p32, const wa_strides* strides, void* out,
+              void* ws, size_t ws_bytes, void* stream) {
+    return prompt_call(q, k, v, p0, n, hi, hq, hkv, d, win, ring, scale, p32, nullptr, 0, strides, out, ws, ws_bytes,
+                       stream);
+}
+
+int wa_prompt_sparse(const void* q, const void* k, const void* v, int32_t p0, int32_t n,
+                     const int32_t* hi, int32_t hq, int32_t hkv, int32_t d, int32_t win, int32_t ring,
+                     float scale, int32_t p32, const int32_t* sel, int32_t nsel, const wa_strides* strides,
+                     void* out, void* ws, size_t ws_bytes, void* stream) {
+    if (!sel) return WA_EINVAL;
+    return prompt_call(q, k, v, p0, n, hi, hq, hkv, d, win, ring, scale, p32, sel, nsel, strides, out, ws, ws_bytes,
+                       stream);
 }
 
 int wa_prep_append(const void* src, const int32_t* pos, int32_t n, int32_t hq, int32_t hkv, int32_t d,

@@ -49,11 +49,15 @@ struct PromptArgs {
     void* out;
     WsHeader* hdr;
     int* flags;      // [n * hq]
+    const int32_t* sel;   // block-sparse form: [n, hkv, nsel] selected 64-key blocks; null otherwise
+    int nsel;
 };
 
-// Float64 re-run of every flagged (row, head); mode 0 = decode, 1 = prompt.
+// Float64 re-run of every flagged (row, head); mode 0 = decode, 1 = prompt, 2 = block-sparse prompt.
 struct RerunArgs {
     int mode;
+    const int32_t* sel;   // mode 2: [rows, hkv, nsel] selected 64-key blocks
+    int nsel;
     const void* q;
     const void* k;
     const void* v;
@@ -85,6 +89,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_prompt(const PromptArgs& a, cudaStream_t s);
+cudaError_t launch_prompt_sparse(const PromptArgs& a, cudaStream_t s);
+cudaError_t prompt_sparse_prepare_device(int dev);
 cudaError_t launch_rerun(const RerunArgs& a, cudaStream_t s);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t prompt_prepare_device(int dev);

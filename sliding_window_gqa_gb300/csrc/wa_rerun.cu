@@ -5,6 +5,10 @@
 // row and head as the review thread settles (the block-wide OR made a finite
 // row's bits depend on where a chunk boundary fell).
 //
+// The block-sparse prompt (mode 2) re-runs over the row's visible keys that lie
+// in its selected 64-key blocks (TensorFold pull request #1622); a row with none
+// gets 0 / 0 = NaN, as the formula's empty sums give.
+//
 // One CTA takes one flagged (row, head) at a time.  Pass 1 finds the
 // NaN-propagating maximum score; pass 2 forms w_j = exp(s_j - M) block by
 // block and accumulates sum_j w_j v_j in key order, one thread per output
@@ -68,6 +72,8 @@ __global__ void __launch_bounds__(kRerunThreads) rerun_f64_kernel(RerunArgs a) {
     __shared__ double qd[256];
     __shared__ double wb[kRerunThreads];
     __shared__ double red[kRerunThreads / 32];
+    __shared__ int sel_row[64];
+    __shared__ unsigned char vis[kRerunThreads];
     const int nflag = *reinterpret_cast<volatile int*>(&a.hdr->nflag);
     const int t = threadIdx.x;
     const int G = a.hq / a.hkv;
@@ -108,11 +114,21 @@ __global__ void __launch_bounds__(kRerunThreads) rerun_f64_kernel(RerunArgs a) {
             orow = out + row * a.o_tok + static_cast<int64_t>(h) * d;
         }
         if (t < d) qd[t] = bf16_bits_to_f64(qrow[t]);
+        const int nsel = a.mode == 2 ? a.nsel : 0;
+        if (t < nsel) sel_row[t] = a.sel[(static_cast<int64_t>(row) * a.hkv + g) * a.nsel + t];
         __syncthreads();
+        // mode 2: key j counts only if its block j / 64 is selected
+        auto selected = [&](int j) {
+            if (a.mode != 2) return true;
+            bool hit = false;
+            for (int e = 0; e < nsel; ++e) hit |= sel_row[e] == (j >> 6);
+            return hit;
+        };
 
         // pass 1: the maximum score (NaN if any score is NaN)
         double mloc = -INFINITY;
         for (int j = lo + t; j <= last; j += kRerunThreads) {
+            if (!selected(j)) continue;
             const uint16_t* kr = kb + static_cast<int64_t>(j % a.ring) * kst;
             double s = 0.0;
             for (int e = 0; e < d; ++e) s = s + qd[e] * bf16_bits_to_f64(kr[e]);
@@ -126,7 +142,8 @@ __global__ void __launch_bounds__(kRerunThreads) rerun_f64_kernel(RerunArgs a) {
         for (int base = lo; base <= last; base += kRerunThreads) {
             const int j = base + t;
             double w = 0.0;
-            if (j <= last) {
+            const bool use = j <= last && selected(j);
+            if (use) {
                 const uint16_t* kr = kb + static_cast<int64_t>(j % a.ring) * kst;
                 double s = 0.0;
                 for (int e = 0; e < d; ++e) s = s + qd[e] * bf16_bits_to_f64(kr[e]);
@@ -135,11 +152,13 @@ __global__ void __launch_bounds__(kRerunThreads) rerun_f64_kernel(RerunArgs a) {
                 lloc = lloc + w;
             }
             wb[t] = w;
+            vis[t] = use ? 1 : 0;
             __syncthreads();
             if (t < d) {
                 const int cnt = min(kRerunThreads, last - base + 1);
                 for (int jj = 0; jj < cnt; ++jj)
-                    acc = acc + wb[jj] * bf16_bits_to_f64(vb[static_cast<int64_t>((base + jj) % a.ring) * vst + t]);
+                    if (vis[jj])
+                        acc = acc + wb[jj] * bf16_bits_to_f64(vb[static_cast<int64_t>((base + jj) % a.ring) * vst + t]);
             }
             __syncthreads();
         }

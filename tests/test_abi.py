@@ -117,6 +117,26 @@ def test_prep_append_argument_errors_before_any_cuda_call():
     assert call(ws_bytes=128) == wa.WA_EWORKSPACE
 
 
+def test_prompt_sparse_argument_errors():
+    wa = ensure_built()
+    L = wa.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    E = wa.WA_EINVAL
+
+    def call(**kw):
+        a = dict(p0=1300, n=512, hq=16, hkv=8, d=256, win=1024, ring=1536, p32=1, sel=fake, nsel=32, ws_bytes=1 << 30)
+        a.update(kw)
+        return L.wa_prompt_sparse(fake, fake, fake, a["p0"], a["n"], None, a["hq"], a["hkv"], a["d"], a["win"],
+                                  a["ring"], 1.0, a["p32"], a["sel"], a["nsel"], None, fake, fake, a["ws_bytes"], None)
+
+    assert call(sel=None) == E
+    assert call(nsel=0) == E
+    assert call(nsel=65) == E
+    assert call(p32=3) == E
+    assert call(win=0, ring=5_000_000, p0=0, n=4_500_000) == E   # key span over 65,536 blocks
+    assert call(ws_bytes=8) == wa.WA_EWORKSPACE
+
+
 def test_strerror_and_version():
     wa = ensure_built()
     L = wa.lib()
