@@ -17,7 +17,10 @@ default step): decode_gqa8 (decode_sliding with 32 query heads over 4 key
 heads) and decode_gqa16_linear (decode_linear with 32 over 2), the groups the
 tensor-core decode serves.  prep_dense (optional too) is the dense workload's
 q/k preparation: per-head RMSNorm of Q and K in place in the interleaved QKV
-buffer (37,810 tokens, 56 heads, d 128), HBM-bound.
+buffer (37,810 tokens, 56 heads, d 128), HBM-bound.  prompt_sparse (optional)
+is the block-sparse prompt of TensorFold #1622's shapes: 7,936 causal rows, 24/2
+heads, d 256, each row's 2,048 selected keys as 32 blocks of 64, three-part P;
+its flops count the visible selected keys only.
 
 value = (decode bytes / HBM peak + prompt flops / bf16 peak) / measured step time:
 the step's roofline time over its measured time.  Decode bytes are the visible
@@ -50,7 +53,7 @@ UNIT = "fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 PARTS = ("decode_sliding", "decode_linear", "prompt_causal", "prompt_dense")
-EXTRA_PARTS = ("decode_gqa8", "decode_gqa16_linear", "prep_dense")
+EXTRA_PARTS = ("decode_gqa8", "decode_gqa16_linear", "prep_dense", "prompt_sparse")
 SPEC = {
     "decode_sliding": dict(caches=3, rows=64, hq=32, hkv=16, d=256, win=1024, ring=1536, pos_max=40000,
                            seed=20260003),
@@ -61,6 +64,7 @@ SPEC = {
                         seed=20260007),
     "decode_gqa16_linear": dict(rows=64, hq=32, hkv=2, d=256, win=0, ring=32768, seed=20260008),
     "prep_dense": dict(N=37810, H=56, d=128, seed=20260009),
+    "prompt_sparse": dict(n=7936, p0=0, hq=24, hkv=2, d=256, win=0, ring=7936, nsel=32, p32=2, seed=20260010),
 }
 
 # ncu DRAM bytes per launch of the dominant kernels, valid only while the kernel source is unchanged.
@@ -113,11 +117,43 @@ def prompt_flops_rows(rows, p0, win, hi_of, hq, d) -> int:
     return tot * hq * 4 * d
 
 
+_SEL_CACHE: dict = {}
+
+
+def sparse_selection_of(s):
+    """The part's synthetic block selection [n, hkv, nsel] (CPU int32), generated once."""
+    import wa_synth
+    key = (s["n"], s["p0"], s["hkv"], s["nsel"], s["seed"], s["win"])
+    if key not in _SEL_CACHE:
+        _SEL_CACHE[key] = wa_synth.sparse_selection(s["n"], s["p0"], s["hkv"], s["nsel"], seed=s["seed"], win=s["win"])
+    return _SEL_CACHE[key]
+
+
+def sparse_visible_keys(s):
+    """Visible selected keys per (row, key head): blocks counted once, cut to [lo, p]."""
+    import numpy as np
+    sel = sparse_selection_of(s).numpy().astype(np.int64)
+    n = s["n"]
+    p = (s["p0"] + np.arange(n))[:, None, None]
+    lo = np.maximum(0, p - s["win"] + 1) if s["win"] > 0 else np.zeros_like(p)
+    srt = np.sort(sel, axis=2)
+    first = np.ones_like(srt, dtype=bool)
+    first[:, :, 1:] = srt[:, :, 1:] != srt[:, :, :-1]
+    a = np.maximum(lo, srt * 64)
+    e = np.minimum(p, srt * 64 + 63)
+    cnt = np.where((srt >= 0) & first & (e >= a), e - a + 1, 0)
+    return cnt.sum(axis=2)
+
+
 def part_work(part: str):
     s = SPEC[part]
     if part.startswith("decode"):
         return {"bytes": sum(decode_bytes(p, s["hq"], s["hkv"], s["d"], s["win"]) for p in decode_positions(part)),
                 "flops": 0}
+    if part == "prompt_sparse":
+        vis = sparse_visible_keys(s)
+        return {"bytes": 0, "flops": int(vis.sum()) * (s["hq"] // s["hkv"]) * 4 * s["d"],
+                "issued_flops_factor": 2.0 if s["p32"] == 2 else (1.5 if s["p32"] else 1.0)}
     if part == "prep_dense":
         # Q and K heads read once and written once (V stays in place)
         return {"bytes": 2 * s["N"] * 2 * s["H"] * s["d"] * 2, "flops": 0}
@@ -415,6 +451,44 @@ class PrepDense(Part):
         return {"qkv": self.qkv.cpu().pin_memory(), "out": torch_empty_pinned_like(self.qkv)}
 
 
+class PromptSparse(Part):
+    name = "prompt_sparse"
+
+    def __init__(self, torch, wa, wa_synth, dev):
+        s = SPEC[self.name]
+        self.torch, self.wa = torch, wa
+        self.c = wa_synth.prompt_case(s["n"], s["p0"], s["hq"], s["hkv"], s["d"], s["win"], s["ring"],
+                                      seed=s["seed"], device=dev, outside="keep")
+        self.sel = sparse_selection_of(s).to(dev)
+        self.out = torch.empty_like(self.c["q"])
+        self.ws = torch.empty(wa.prompt_ws_bytes(s["n"], s["hq"]), dtype=torch.uint8, device=dev)
+        self.launches = 2   # sparse prompt kernel, float64 re-run
+        self.k_start, self.k_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.kernel_ms = []
+
+    def run(self, stream, host=None):
+        s, c = SPEC[self.name], self.c
+        if host is not None:
+            for key in ("q", "k", "v"):
+                c[key].copy_(host[key], non_blocking=True)
+            self.sel.copy_(host["sel"], non_blocking=True)
+        self.k_start.record(stream)
+        self.wa.prompt_sparse(c["q"], c["k"], c["v"], s["p0"], self.sel, None, s["win"], 1.0, p32=s["p32"],
+                              out=self.out, ws=self.ws, stream=stream)
+        self.k_end.record(stream)
+        if host is not None:
+            host["out"].copy_(self.out, non_blocking=True)
+
+    def collect(self):
+        self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
+
+    def host_buffers(self):
+        d = {k: self.c[k].cpu().pin_memory() for k in ("q", "k", "v")}
+        d["sel"] = self.sel.cpu().pin_memory()
+        d["out"] = torch_empty_pinned_like(self.out)
+        return d
+
+
 class DecodeGqa8(DecodeSliding):
     name = "decode_gqa8"
 
@@ -425,18 +499,20 @@ class DecodeGqa16Linear(DecodeLinear):
 
 PART_CLASSES = {"decode_sliding": DecodeSliding, "decode_linear": DecodeLinear,
                 "prompt_causal": PromptCausal, "prompt_dense": PromptDense,
-                "decode_gqa8": DecodeGqa8, "decode_gqa16_linear": DecodeGqa16Linear, "prep_dense": PrepDense}
+                "decode_gqa8": DecodeGqa8, "decode_gqa16_linear": DecodeGqa16Linear, "prep_dense": PrepDense,
+                "prompt_sparse": PromptSparse}
 
 KERNEL_OF = {"decode_sliding": "decode partial (wa_decode.cu)", "decode_linear": "decode partial (wa_decode.cu)",
              "prompt_causal": "prompt tensor-core tile (wa_prompt.cu)",
              "prompt_dense": "prompt tensor-core tile (wa_prompt.cu)",
              "decode_gqa8": "tensor-core decode partial (wa_decode_tc.cu)",
              "decode_gqa16_linear": "tensor-core decode partial (wa_decode_tc.cu)",
-             "prep_dense": "q/k preparation (wa_prep.cu)"}
+             "prep_dense": "q/k preparation (wa_prep.cu)",
+             "prompt_sparse": "block-sparse prompt tile (wa_prompt_sparse.cu)"}
 SOURCE_OF = {"decode_sliding": "wa_decode.cu", "decode_linear": "wa_decode.cu",
              "prompt_causal": "wa_prompt.cu", "prompt_dense": "wa_prompt.cu",
              "decode_gqa8": "wa_decode_tc.cu", "decode_gqa16_linear": "wa_decode_tc.cu",
-             "prep_dense": "wa_prep.cu"}
+             "prep_dense": "wa_prep.cu", "prompt_sparse": "wa_prompt_kernel.cuh"}
 
 
 def source_hash(fname: str) -> str:
@@ -567,6 +643,10 @@ def _sample_inputs(part: str, i: int = 0):
             c = wa_synth.decode_case(1, s["hq"], s["hkv"], s["d"], s["win"], s["ring"], [p],
                                      seed=s["seed"] + i, outside="keep", peaked=False)
             _SAMPLES[key] = (p, bits(c["q"]), bits(c["k"]), bits(c["v"]))
+        elif part == "prompt_sparse":
+            c = wa_synth.prompt_case(s["n"], s["p0"], s["hq"], s["hkv"], s["d"], s["win"], s["ring"], seed=s["seed"],
+                                     outside="keep", peaked=False)
+            _SAMPLES[key] = (bits(c["q"]), bits(c["k"]), bits(c["v"]), sparse_selection_of(s).numpy())
         elif part == "prep_dense":
             g = torch.Generator().manual_seed(s["seed"])
             x = torch.randn((1024, 3 * s["H"] * s["d"]), generator=g).to(torch.bfloat16)
@@ -607,6 +687,20 @@ def oracle_sample(parts, budget_s: float):
                 rows_done += 1
             total += t_used * w["bytes"] / work_done
             desc.append(f"{part}: {rows_done} rows of {n_rows}")
+        elif part == "prompt_sparse":
+            q, k, v, sel = _sample_inputs(part)
+            vis = sparse_visible_keys(s)
+            rng = np.random.default_rng(s["seed"])
+            rows_done, t_used, flops_done = 0, 0.0, 0
+            while t_used < per and rows_done < 64:
+                i = int(rng.integers(0, s["n"]))
+                t0 = time.perf_counter()
+                oracle.prompt_sparse(q, k, v, s["p0"], s["win"], s["ring"], 1.0, sel, rows=[i])
+                t_used += time.perf_counter() - t0
+                flops_done += int(vis[i].sum()) * (s["hq"] // s["hkv"]) * 4 * s["d"]
+                rows_done += 1
+            total += t_used * w["flops"] / flops_done
+            desc.append(f"{part}: {rows_done} random rows of {s['n']}, all heads")
         elif part == "prep_dense":
             from oracle import prep
             (x,) = _sample_inputs(part)

@@ -322,6 +322,14 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = misc[0];
+    if (warp == 0 && lane == 0) {   // Q first: it needs nothing the rest of the set-up computes
+        prefetch_tensormap(&p.tq);
+        prefetch_tensormap(&p.tk);
+        prefetch_tensormap(&p.tv);
+        mbar_arrive_expect_tx(BAR(B_Q), C::KB * gsz * nrows * 128);   // the box: 64 dims x gsz x nrows
+        for (int b = 0; b < C::KB; ++b)
+            tma_load_3d(sbase + C::OFF_Q + b * C::Q_BLOCK, &p.tq, b * 64, h0, m0, BAR(B_Q), policy_evict_first());
+    }
     int ulo = INT_MAX, uhi = INT_MIN;
     for (int w = 0; w < 4; ++w) {
         ulo = min(ulo, static_cast<int>(misc[1 + w]));
@@ -335,24 +343,44 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
     const uint16_t* my_list = sel_lists + rl * kSelMax;
     if constexpr (SP) {
         if (warp >= 4 && warp < 8 && lane_ok && h == h0) {
+            // the row's entries, all loads first; blocks with no visible key become 0xFFFF
             uint16_t* lst = sel_lists + rl * kSelMax;
             const int32_t* srow = p.sel + (static_cast<int64_t>(i) * p.hkv + g) * p.nsel;
             const int blo = row_lo / T, bhi = row_hi / T;
-            int cnt = 0;
-            for (int e = 0; e < p.nsel; ++e) {
-                const int b = srow[e];
-                if (b < blo || b > bhi) continue;   // unused (< 0) or no visible key in the block
-                const int rel = b - j0s;
-                bool dup = false;
-                for (int q = 0; q < cnt; ++q) dup |= lst[q] == rel;
-                if (dup) continue;
-                int pos = cnt++;
-                while (pos > 0 && lst[pos - 1] > rel) {
-                    lst[pos] = lst[pos - 1];
-                    --pos;
+            uint32_t v[kSelMax];
+#pragma unroll
+            for (int e = 0; e < kSelMax; ++e) {
+                const int b = e < p.nsel ? srow[e] : -1;
+                v[e] = (b >= blo && b <= bhi) ? static_cast<uint32_t>(b - j0s) : 0xFFFFu;
+            }
+            // ascending bitonic sort in registers (compile-time indices)
+#pragma unroll
+            for (int k = 2; k <= kSelMax; k <<= 1) {
+#pragma unroll
+                for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+                    for (int e = 0; e < kSelMax; ++e) {
+                        const int l = e ^ j;
+                        if (l > e) {
+                            const uint32_t lo = min(v[e], v[l]), hi = max(v[e], v[l]);
+                            const bool up = (e & k) == 0;
+                            v[e] = up ? lo : hi;
+                            v[l] = up ? hi : lo;
+                        }
+                    }
                 }
-                lst[pos] = static_cast<uint16_t>(rel);
-                atomicOr(&bmap[rel >> 5], 1u << (rel & 31));
+            }
+            // repeats dropped; the union gains each block
+            int cnt = 0;
+            uint32_t prev = 0xFFFFFFFFu;
+#pragma unroll
+            for (int e = 0; e < kSelMax; ++e) {
+                const uint32_t x = v[e];
+                if (x != 0xFFFFu && x != prev) {
+                    lst[cnt++] = static_cast<uint16_t>(x);
+                    atomicOr(&bmap[x >> 5], 1u << (x & 31));
+                }
+                prev = x;
             }
             sel_cnt[rl] = cnt;
         }
@@ -363,16 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
-        const uint64_t pol_q = policy_evict_first();
         const uint64_t pol_kv = policy_evict_last();
-        if (lane == 0) {
-            prefetch_tensormap(&p.tq);
-            prefetch_tensormap(&p.tk);
-            prefetch_tensormap(&p.tv);
-            mbar_arrive_expect_tx(BAR(B_Q), C::KB * gsz * nrows * 128);   // the box: 64 dims x gsz x nrows
-            for (int b = 0; b < C::KB; ++b)
-                tma_load_3d(sbase + C::OFF_Q + b * C::Q_BLOCK, &p.tq, b * 64, h0, m0, BAR(B_Q), pol_q);
-        }
         bool ok = true;
         int issued = 0;
         TileWalk<SP> tiles;
