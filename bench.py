@@ -800,13 +800,14 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=4.0, help="oracle seconds per reference step")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="oracle seconds for cpu_baseline")
     ap.add_argument("--caches", type=int, default=None, help="override the decode_sliding cache count (profiling)")
-    ap.add_argument("--dense-n", type=int, default=None, help="override the prompt_dense row count (profiling)")
+    ap.add_argument("--dense-n", type=int, default=None, help="override the prompt_dense and prep_dense row count (profiling)")
     ap.add_argument("--decode-rows", type=int, default=None, help="override every decode part's rows per cache (profiling)")
     args = ap.parse_args()
     if args.caches is not None:
         SPEC["decode_sliding"]["caches"] = args.caches
     if args.dense_n is not None:
         SPEC["prompt_dense"]["N"] = args.dense_n
+        SPEC["prep_dense"]["N"] = args.dense_n
     if args.decode_rows is not None:
         for name, sp in SPEC.items():
             if name.startswith("decode"):
