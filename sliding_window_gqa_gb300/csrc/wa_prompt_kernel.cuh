@@ -264,8 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             mbar_init(BAR(B_KFULL + s), 1);
             mbar_init(BAR(B_VFULL + s), 1);
             mbar_init(BAR(B_VREADY + s), 1);
-            mbar_init(BAR(B_KFREE + s), 1);
-            mbar_init(BAR(B_VFREE + s), 1);
             mbar_init(BAR(B_SFULL + s), 1);
             mbar_init(BAR(B_SFREE + s), 8);
             mbar_init(BAR(B_XCHG + s), 8);      // one arrival per softmax warp
@@ -404,7 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             for (int kv = 0; kv < 2 && ok; ++kv) {
                 const uint32_t full = BAR((kv ? B_VFULL : B_KFULL) + s);
                 const uint32_t dst = sbase + (kv ? C::OFF_V : C::OFF_K) + s * C::KV_BYTES;
-                if (u > 0 && !warp_wait(BAR((kv ? B_VFREE : B_KFREE) + s), (u - 1) & 1, p.status)) {
+                // a stage is free once the product that read it is done: S of tile idx - 2 for K,
+                // P.V of tile idx - 2 for V (their commits are the only ones the MMA warp issues)
+                if (u > 0 && !warp_wait(BAR((kv ? B_PVDONE : B_SFULL) + s), (u - 1) & 1, p.status)) {
                     ok = false;
                     break;
                 }
@@ -444,15 +444,15 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
                     if (ok && idx >= 2) ok = mbar_wait(BAR(B_SFREE + s), (u - 1) & 1, p.status);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t kst = sbase + C::OFF_K + s * C::KV_BYTES;
+                    // descriptors built once; step kk moves the start address (16-byte units) by a constant
+                    const uint64_t a0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+                    const uint64_t b0 = sdesc_sw128(sbase + C::OFF_K + s * C::KV_BYTES, 16, 1024);
+                    const uint32_t d_s = tbase + C::S_COL + s * T;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t a = sdesc_sw128(sbase + C::OFF_Q + (kk >> 2) * C::Q_BLOCK + (kk & 3) * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(kst + (kk >> 2) * C::KV_BLOCK + (kk & 3) * 32, 16, 1024);
-                        mma_bf16_ss(tbase + C::S_COL + s * T, a, b, idS, kk > 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_bf16_ss(d_s, a0 + (((kk >> 2) * C::Q_BLOCK + (kk & 3) * 32) >> 4),
+                                    b0 + (((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
                     mma_commit(BAR(B_SFULL + s));
-                    mma_commit(BAR(B_KFREE + s));
                 }
                 if (idx >= 1) {
                     const int pidx = idx - 1, ps = pidx & 1, pu = pidx >> 1;
@@ -460,18 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
                     if (ok) ok = mbar_wait(BAR(B_VREADY + ps), pu & 1, p.status);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t vst = sbase + C::OFF_V + ps * C::KV_BYTES;
+                    const uint64_t v0 = sdesc_sw128(sbase + C::OFF_V + ps * C::KV_BYTES, C::KV_BLOCK, 1024);
 #pragma unroll
                     for (int half = 0; half < NP; ++half) {
                         const uint32_t pt = tbase + C::p_col(NP > 1 ? half : (pidx & 1));
 #pragma unroll
-                        for (int kk = 0; kk < T / 16; ++kk) {
-                            const uint64_t b = sdesc_sw128(vst + kk * 16 * 128, C::KV_BLOCK, 1024);
-                            mma_bf16_ts(tbase + C::O_COL, pt + kk * 8, b, idO, (pidx > 0 || kk > 0 || half > 0) ? 1u : 0u);
-                        }
+                        for (int kk = 0; kk < T / 16; ++kk)
+                            mma_bf16_ts(tbase + C::O_COL, pt + kk * 8, v0 + ((kk * 16 * 128) >> 4), idO,
+                                        (pidx > 0 || kk > 0 || half > 0) ? 1u : 0u);
                     }
                     mma_commit(BAR(B_PVDONE + (pidx & 1)));
-                    mma_commit(BAR(B_VFREE + ps));
                 }
             }
             // every MMA issued so far has finished before tensor memory can be released
@@ -521,9 +519,6 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             tc_fence_after();
             float sv[NC];
             load_s<NC>(tbase + lane_addr + C::S_COL + s * T + col0, sv);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_SFREE + s));
 
             // visible columns of this half: [vlo, vhi]; interior tiles need no mask at all
             const int rel = tiles.next();
@@ -555,6 +550,36 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             xs[wg * kBM + r] = mh;
             __syncwarp();   // the warp's stores precede lane 0's (cumulative) release
             if (lane == 0) mbar_arrive(BAR(B_XCHG + (idx & 1)));
+            float ls8[8];
+            // p = 2^(S c - m_sub) into sv, and the row sum in ls8
+            auto exponents = [&](float m_sub) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ls8[e] = 0.f;
+                if (masked) {   // a masked column is 0 whatever its score (also for scale 0 or a NaN key)
+#pragma unroll
+                    for (int k = 0; k < NC; ++k) {
+                        const float pk = (k >= vlo && k <= vhi) ? ex2(fmaf(sv[k], c, -m_sub)) : 0.f;
+                        sv[k] = pk;
+                        ls8[k & 7] += pk;
+                    }
+                } else {   // two columns per packed FMA and packed add
+#pragma unroll
+                    for (int k = 0; k < NC; k += 2) {
+                        float x0, x1;
+                        fma_x2(x0, x1, sv[k], sv[k + 1], c, c, -m_sub, -m_sub);
+                        sv[k] = ex2(x0);
+                        sv[k + 1] = ex2(x1);
+                        const int j = (k >> 1) & 3;
+                        add_x2(ls8[2 * j], ls8[2 * j + 1], sv[k], sv[k + 1]);
+                    }
+                }
+            };
+            // The lazy rule usually keeps the running max, so the exponentials start with it while
+            // the other half's maximum is on its way; a warp in which any row's max moves redoes
+            // them from the S buffer (still held: SFREE comes after).  The values are those of the
+            // rule's own m either way.
+            const bool spec = __all_sync(0xFFFFFFFFu, m_run != -INFINITY && mh * c <= m_run + kLazy);
+            if (spec) exponents(m_run);
             if (!warp_wait(BAR(B_XCHG + (idx & 1)), (idx >> 1) & 1, p.status)) { ok = false; break; }
             const float mraw = fmaxf(xs[r], xs[kBM + r]);   // the same order in both halves
             const float mt = mraw * c;                       // tile max in log2 units
@@ -562,27 +587,13 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             const float m_new = (mt > m_run + kLazy) ? mt : m_run;
             const float alpha = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
             const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
-            float ls8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ls8[e] = 0.f;
-            if (masked) {   // a masked column is 0 whatever its score (also for scale 0 or a NaN key)
-#pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    const float pk = (k >= vlo && k <= vhi) ? ex2(fmaf(sv[k], c, -m_sub)) : 0.f;
-                    sv[k] = pk;
-                    ls8[k & 7] += pk;
-                }
-            } else {   // two columns per packed FMA and packed add
-#pragma unroll
-                for (int k = 0; k < NC; k += 2) {
-                    float x0, x1;
-                    fma_x2(x0, x1, sv[k], sv[k + 1], c, c, -m_sub, -m_sub);
-                    sv[k] = ex2(x0);
-                    sv[k + 1] = ex2(x1);
-                    const int j = (k >> 1) & 3;
-                    add_x2(ls8[2 * j], ls8[2 * j + 1], sv[k], sv[k + 1]);
-                }
+            if (!spec || __any_sync(0xFFFFFFFFu, m_new != m_run)) {
+                if (spec) load_s<NC>(tbase + lane_addr + C::S_COL + s * T + col0, sv);
+                exponents(m_sub);
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_SFREE + s));
             const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
             l_run = (alpha == 1.f) ? (l_run + lsum) : fmaf(l_run, alpha, lsum);
             m_run = m_new;
