@@ -69,8 +69,8 @@ SPEC = {
 
 # ncu DRAM bytes per launch of the dominant kernels, valid only while the kernel source is unchanged.
 TRAFFIC = {
-    "prompt_dense": {"bytes_per_launch": 2070 * 10**6, "source_sha": "1e0dfa0763edd056",
-                     "note": "ncu at N=8192 (352.4 MB read + 96.1 MB write), scaled by N to 37,810"},
+    "prompt_dense": {"bytes_per_launch": 2068 * 10**6, "source_sha": "168bcbfa1a37d5a6",
+                     "note": "ncu at N=8192 (352.4 MB read + 95.6 MB write), scaled by N to 37,810"},
     "decode_gqa8": {"bytes_per_launch": 853 * 10**6, "source_sha": "2033d7ed7d9eaec4",
                     "note": "the part's three launches together, like its achieved figure: ncu at 256 rows, one cache "
                             "(1.134 GB read + 8.0 MB write for 1.072 GB algorithmic), scaled by algorithmic bytes "
@@ -503,14 +503,14 @@ PART_CLASSES = {"decode_sliding": DecodeSliding, "decode_linear": DecodeLinear,
                 "prompt_sparse": PromptSparse}
 
 KERNEL_OF = {"decode_sliding": "decode partial (wa_decode.cu)", "decode_linear": "decode partial (wa_decode.cu)",
-             "prompt_causal": "prompt tensor-core tile (wa_prompt.cu)",
-             "prompt_dense": "prompt tensor-core tile (wa_prompt.cu)",
+             "prompt_causal": "prompt tensor-core tile (wa_prompt_kernel.cuh)",
+             "prompt_dense": "prompt tensor-core tile (wa_prompt_kernel.cuh)",
              "decode_gqa8": "tensor-core decode partial (wa_decode_tc.cu)",
              "decode_gqa16_linear": "tensor-core decode partial (wa_decode_tc.cu)",
              "prep_dense": "q/k preparation (wa_prep.cu)",
              "prompt_sparse": "block-sparse prompt tile (wa_prompt_sparse.cu)"}
 SOURCE_OF = {"decode_sliding": "wa_decode.cu", "decode_linear": "wa_decode.cu",
-             "prompt_causal": "wa_prompt.cu", "prompt_dense": "wa_prompt.cu",
+             "prompt_causal": "wa_prompt_kernel.cuh", "prompt_dense": "wa_prompt_kernel.cuh",
              "decode_gqa8": "wa_decode_tc.cu", "decode_gqa16_linear": "wa_decode_tc.cu",
              "prep_dense": "wa_prep.cu", "prompt_sparse": "wa_prompt_kernel.cuh"}
 
