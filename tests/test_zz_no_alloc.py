@@ -64,6 +64,18 @@ def test_static_matches_workspace_entry_two_calls_in_a_row(wa):
         assert torch.equal(torch.isnan(got.float()), torch.isnan(want.float()))
 
 
+def test_static_tensor_core_decode_gives_the_workspace_bits(wa):
+    """Groups of 8 query heads per key head take the tensor-core partial kernel; over the
+    library-owned scratch it must give the workspace entry's bits."""
+    stream = torch.cuda.current_stream()
+    c = _dev(wa_synth.decode_case(4, 32, 4, 256, 1024, 1536, [1535, 700, 40000, 2049], seed=74))
+    want = wa.decode(c["q"], c["k"], c["v"], c["pos"], 1024, 1.0)
+    got = torch.empty_like(want)
+    assert _static(wa, c, 1024, got, stream) == wa.WA_OK
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
 def wa_synth_value(t):
     return t.float().cpu().numpy().astype(np.float64)
 
