@@ -63,8 +63,9 @@ REL_L2ROPE = 2.0 ** -6
 def rmsnorm_head(x: np.ndarray) -> np.ndarray:
     """x / sqrt(mean(x^2) + 1e-5) along the last axis, float64."""
     x = np.asarray(x, dtype=np.float64)
-    ms = np.mean(x * x, axis=-1, keepdims=True)
-    return x / np.sqrt(ms + RMS_EPS)
+    with np.errstate(invalid="ignore", over="ignore"):   # IEEE classes pass through as the formula says
+        ms = np.mean(x * x, axis=-1, keepdims=True)
+        return x / np.sqrt(ms + RMS_EPS)
 
 
 def rope_angle32(pos: int, inv_freq32: np.ndarray) -> np.ndarray:
@@ -87,7 +88,8 @@ def rope_rotate_half(x: np.ndarray, ang: np.ndarray) -> np.ndarray:
 def l2_head(x: np.ndarray) -> np.ndarray:
     """x * (1 / sqrt(sum(x^2) + 1e-6)) along the last axis, float64."""
     x = np.asarray(x, dtype=np.float64)
-    return x * (1.0 / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + L2_EPS))
+    with np.errstate(invalid="ignore", over="ignore"):
+        return x * (1.0 / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + L2_EPS))
 
 
 def _rn(x):
@@ -146,8 +148,9 @@ def prepare(src_bits, pos, hq: int, hkv: int, d: int, mode: str, q_scale=None, i
         if with_allowance:
             for r64, xh, sc, o, tol in ((rq64, xq[t], qs, q_out[t], q_tol), (rk64, xk[t], 1.0, k_out[t], k_tol)):
                 e = _rotation_bound(xh, ang)
-                norm = np.sqrt(np.sum(_rn(r64) ** 2, axis=-1, keepdims=True) + L2_EPS)
-                tol[t] = REL_L2ROPE * np.abs(o) + sc * (e + _ulp_bf16(np.abs(r64) + e)) / norm
+                with np.errstate(invalid="ignore", over="ignore"):
+                    norm = np.sqrt(np.sum(_rn(r64) ** 2, axis=-1, keepdims=True) + L2_EPS)
+                    tol[t] = REL_L2ROPE * np.abs(o) + sc * (e + _ulp_bf16(np.abs(r64) + e)) / norm
     if with_allowance:
         return q_out, k_out, v_bits, q_tol, k_tol
     return q_out, k_out, v_bits

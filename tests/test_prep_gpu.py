@@ -207,3 +207,40 @@ def test_bits_do_not_depend_on_the_batch(wa):
         qb, kb = run(sel)
         assert torch.equal(qb.view(torch.int16), qa[sel].view(torch.int16))
         assert torch.equal(kb.view(torch.int16), ka[sel].view(torch.int16))
+
+
+def test_positions_past_2_to_24(wa):
+    """fl32(pos) itself rounds above 2^24; the angle is fl32(fl32(pos) * inv) on both sides."""
+    pos = [2**24 - 1, 2**24 + 1, 2**25 + 3, 123_456_789, 2**31 - 1]
+    _run_decode_layout(wa, len(pos), 16, 4, 256, 4096, pos, "l2_rope", seed=81)
+
+
+@pytest.mark.parametrize("mode", ["rmsnorm", "l2_rope"])
+def test_nonfinite_projections_follow_float64(wa, mode):
+    n, hq, hkv, d, ring = 6, 8, 2, 128, 64
+    src = _src(n, hq, hkv, d, 91)
+    src[1, 5] = float("nan")                      # query head 0 of token 1
+    src[2, hq * d + 7] = float("inf")             # key head 0 of token 2
+    src[3, 3 * d + 1] = float("-inf")             # query head 3 of token 3
+    src[4, (hq + hkv) * d + 2] = float("nan")     # a value: copied as is
+    q_out = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
+    k_ring = torch.zeros((n, ring, hkv, d), dtype=torch.bfloat16, device="cuda")
+    v_ring = torch.zeros_like(k_ring)
+    qs, inv = _mode_args(mode, d, 92)
+    pos = [1, 2, 3, 4, 5, 6]
+    ws = wa.prep_append(src, torch.tensor(pos, dtype=torch.int32, device="cuda"), q_out, k_ring, v_ring, mode=mode,
+                        q_scale=None if qs is None else torch.from_numpy(qs).cuda(),
+                        inv_freq=None if inv is None else torch.from_numpy(inv).cuda())
+    assert wa.status(ws) == 0
+    q_ref, k_ref, v_bits, tq, tk = _reference(src, pos, hq, hkv, d, mode, qs, inv)
+    assert np.isnan(q_ref[1, 0]).any() and not np.isfinite(k_ref[2, 0]).all()
+    with np.errstate(invalid="ignore"):
+        tq = np.nan_to_num(tq, nan=0.0) if not np.isscalar(tq) else tq
+        tk = np.nan_to_num(tk, nan=0.0) if not np.isscalar(tk) else tk
+    rq = prep.check_prep(bits(q_out), q_ref, tq)
+    assert rq["ok"], rq
+    sl = torch.arange(n, device="cuda")
+    slots = torch.tensor(pos, device="cuda") % ring
+    rk = prep.check_prep(bits(k_ring[sl, slots]), k_ref, tk)
+    assert rk["ok"], rk
+    assert np.array_equal(bits(v_ring[sl, slots]), v_bits)
