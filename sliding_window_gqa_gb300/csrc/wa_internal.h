@@ -96,7 +96,7 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t prompt_prepare_device(int dev);
 cudaError_t decode_prepare_device(int dev);
 // Decode partials on the tensor cores (query-head groups of kTcMinGroup and more); the merge is shared.
-constexpr int kTcMinGroup = 4;
+constexpr int kTcMinGroup = 3;
 cudaError_t launch_decode_tc_part(const DecodeArgs& a, cudaStream_t s);
 cudaError_t decode_tc_prepare_device(int dev);
 
