@@ -51,7 +51,7 @@ CASES = [
     ("gqa16_d128", 17, 32, 2, 128, 1024, 1536, list(range(100, 40000, 2350))[:17]),
     ("one_key_window", 2, 4, 2, 256, 1, 4, [0, 17]),
     ("chunk_edges", 6, 4, 2, 256, 513, 1024, [255, 256, 511, 512, 767, 768]),
-    # groups of 4 and more run on the tensor cores
+    # groups of 3 and more run on the tensor cores
     ("gqa4_ring1000_wrap", 4, 16, 4, 256, 700, 1000, [0, 255, 256, 5000]),
     ("gqa8_linear_d256", 3, 16, 2, 256, 0, 2000, [0, 1023, 1999]),
     ("gqa4_d128_chunk_edges", 6, 8, 2, 128, 513, 1024, [255, 256, 511, 512, 767, 768]),
