@@ -198,6 +198,49 @@ __device__ __forceinline__ void load_s(uint32_t taddr, float (&sv)[NC]) {
     }
 }
 
+// Block-sparse: one row's selected blocks that hold a visible key ([blo, bhi]), relative to j0,
+// sorted and without repeats, into lst; each also set in the CTA's union bitmap.  All N entries
+// are loaded first (unused ones as 0xFFFF, which sorts last), then an ascending bitonic network in
+// registers with compile-time indices; N is the smallest of 32 and 64 that holds the row's list.
+template <int N>
+__device__ __forceinline__ int build_block_list(const int32_t* srow, int nsel, int blo, int bhi, int j0,
+                                                uint16_t* lst, uint32_t* bmap) {
+    uint32_t v[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+        const int b = e < nsel ? srow[e] : -1;
+        v[e] = (b >= blo && b <= bhi) ? static_cast<uint32_t>(b - j0) : 0xFFFFu;
+    }
+#pragma unroll
+    for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+                const int l = e ^ j;
+                if (l > e) {
+                    const uint32_t lo = min(v[e], v[l]), hi = max(v[e], v[l]);
+                    const bool up = (e & k) == 0;
+                    v[e] = up ? lo : hi;
+                    v[l] = up ? hi : lo;
+                }
+            }
+        }
+    }
+    int cnt = 0;
+    uint32_t prev = 0xFFFFFFFFu;
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+        const uint32_t x = v[e];
+        if (x != 0xFFFFu && x != prev) {
+            lst[cnt++] = static_cast<uint16_t>(x);
+            atomicOr(&bmap[x >> 5], 1u << (x & 31));
+        }
+        prev = x;
+    }
+    return cnt;
+}
+
 // Tiles in ascending key order: the dense form walks j0, j0 + 1, ...; the block-sparse form walks
 // the set bits of the CTA's union bitmap.  next() returns the tile's block relative to j0 and is
 // called exactly once per tile.
@@ -341,45 +384,12 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
     const uint16_t* my_list = sel_lists + rl * kSelMax;
     if constexpr (SP) {
         if (warp >= 4 && warp < 8 && lane_ok && h == h0) {
-            // the row's entries, all loads first; blocks with no visible key become 0xFFFF
-            uint16_t* lst = sel_lists + rl * kSelMax;
             const int32_t* srow = p.sel + (static_cast<int64_t>(i) * p.hkv + g) * p.nsel;
-            const int blo = row_lo / T, bhi = row_hi / T;
-            uint32_t v[kSelMax];
-#pragma unroll
-            for (int e = 0; e < kSelMax; ++e) {
-                const int b = e < p.nsel ? srow[e] : -1;
-                v[e] = (b >= blo && b <= bhi) ? static_cast<uint32_t>(b - j0s) : 0xFFFFu;
-            }
-            // ascending bitonic sort in registers (compile-time indices)
-#pragma unroll
-            for (int k = 2; k <= kSelMax; k <<= 1) {
-#pragma unroll
-                for (int j = k >> 1; j > 0; j >>= 1) {
-#pragma unroll
-                    for (int e = 0; e < kSelMax; ++e) {
-                        const int l = e ^ j;
-                        if (l > e) {
-                            const uint32_t lo = min(v[e], v[l]), hi = max(v[e], v[l]);
-                            const bool up = (e & k) == 0;
-                            v[e] = up ? lo : hi;
-                            v[l] = up ? hi : lo;
-                        }
-                    }
-                }
-            }
-            // repeats dropped; the union gains each block
-            int cnt = 0;
-            uint32_t prev = 0xFFFFFFFFu;
-#pragma unroll
-            for (int e = 0; e < kSelMax; ++e) {
-                const uint32_t x = v[e];
-                if (x != 0xFFFFu && x != prev) {
-                    lst[cnt++] = static_cast<uint16_t>(x);
-                    atomicOr(&bmap[x >> 5], 1u << (x & 31));
-                }
-                prev = x;
-            }
+            const int cnt = p.nsel <= kSelMax / 2
+                                ? build_block_list<kSelMax / 2>(srow, p.nsel, row_lo / T, row_hi / T, j0s,
+                                                                sel_lists + rl * kSelMax, bmap)
+                                : build_block_list<kSelMax>(srow, p.nsel, row_lo / T, row_hi / T, j0s,
+                                                            sel_lists + rl * kSelMax, bmap);
             sel_cnt[rl] = cnt;
         }
         __syncthreads();
