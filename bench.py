@@ -51,6 +51,7 @@ if ROOT not in sys.path:
 METRIC = "decode KV-read GB/s and prompt attention TFLOP/s, as fraction of GB300 roofline"
 UNIT = "fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_HBM_GBS = 8000.0   # the ~8 TB/s nominal figure, printed beside the measured-copy fraction
 
 PARTS = ("decode_sliding", "decode_linear", "prompt_causal", "prompt_dense")
 EXTRA_PARTS = ("decode_gqa8", "decode_gqa16_linear", "prep_dense", "prompt_sparse")
@@ -843,10 +844,12 @@ def main():
         ms = per_part_ms[p]
         if w["bytes"]:
             gbs = w["bytes"] / (ms * 1e-3) / 1e9
-            part_report[p] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "bytes": w["bytes"]}
+            part_report[p] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm_gbs"],
+                              "frac_hbm_nominal_8tbs": gbs / NOMINAL_HBM_GBS, "bytes": w["bytes"]}
         else:
             tf = w["flops"] / (ms * 1e-3) / 1e12
             part_report[p] = {"ms": ms, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops_sustained"],
+                              "frac_bf16_burst": tf / pk["bf16_tflops"],
                               "flops": w["flops"], "issued_TFLOP/s": tf * w.get("issued_flops_factor", 1.0)}
     dom = max(parts, key=lambda p: per_part_ms[p])
     w = part_work(dom)
