@@ -6,8 +6,7 @@ the pages' workloads (TensorFold pull request #1123, "Receipt"; the "Exact
 Numerical Contract" page, "Canonical Boundary"):
 
   decode_sliding  3 independent caches x 64 rows, 32/16 heads, d 256, window 1024
-                  over a ring of 1536, positions uniform to 40,000, three streams (the three
-                  calls captured once in a CUDA graph and replayed each step)
+                  over a ring of 1536, positions uniform to 40,000, three streams
   decode_linear   64 rows, 32/16 heads, d 256, linear cache of 32,768 keys
   prompt_causal   8,192 rows at p0 0, 16/8 heads, d 256, linear cache, causal, P32
   prompt_dense    37,810 rows, 56 heads (MHA), d 128, interleaved QKV (row 21,504),
@@ -28,6 +27,10 @@ the step's roofline time over its measured time.  Decode bytes are the visible
 K and V rows plus q and out; prompt flops are 4*d per visible (row, key, head).
 Peaks come from MEASURED_PEAKS.json (the sustained bf16 figure, since each
 kernel runs inside a long step).
+
+Each part's calls are captured once in a CUDA graph and replayed in the timed region (the
+three-stream parts fork and join inside it), as a serving loop would; the e2e leg calls the C
+ABI eagerly with host copies.
 
 Prints one JSON line.  --impl reference times the float64 oracle on the host
 cores on a bounded sample of the same workload instead.
@@ -248,11 +251,44 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- native arm
 
 class Part:
+    """One part of the step.  calls(stream) makes the part's C-ABI calls; in the timed region they
+    are replayed as a CUDA graph captured after one eager call, so the GPU time does not include the
+    host's per-call work (argument checks, tensor-map encoding).  The e2e leg calls them eagerly."""
     name = ""
     launches = 0
+    graph = None
 
-    def run(self, stream):
+    def calls(self, stream):
         raise NotImplementedError
+
+    def timed_calls(self, stream):
+        torch = self.torch
+        if self.graph is None:
+            self.calls(stream)                      # eager once: device attributes, encoder lookup
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            with torch.cuda.graph(g, stream=cap):
+                self.calls(cap)
+            stream.wait_stream(cap)
+            self.graph = g
+            return
+        self.graph.replay()
+
+    def run(self, stream, host=None):
+        if host is not None:
+            self.copy_in(host)
+            self.k_start.record(stream)
+            self.calls(stream)
+            self.k_end.record(stream)
+            self.copy_out(host)
+            return
+        self.k_start.record(stream)
+        self.timed_calls(stream)
+        self.k_end.record(stream)
+
+    def collect(self):
+        self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
 
 
 def _events(torch, stream, n=2):
@@ -359,19 +395,16 @@ class DecodeLinear(Part):
         self.k_start, self.k_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         self.kernel_ms = []
 
-    def run(self, stream, host=None):
+    def calls(self, stream):
         s, c = SPEC[self.name], self.c
-        if host is not None:
-            for key in ("q", "k", "v", "pos"):
-                c[key].copy_(host[key], non_blocking=True)
-        self.k_start.record(stream)
         self.wa.decode(c["q"], c["k"], c["v"], c["pos"], s["win"], 1.0, out=self.out, ws=self.ws, stream=stream)
-        self.k_end.record(stream)
-        if host is not None:
-            host["out"].copy_(self.out, non_blocking=True)
 
-    def collect(self):
-        self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
+    def copy_in(self, host):
+        for key in ("q", "k", "v", "pos"):
+            self.c[key].copy_(host[key], non_blocking=True)
+
+    def copy_out(self, host):
+        host["out"].copy_(self.out, non_blocking=True)
 
     def host_buffers(self):
         d = {k: self.c[k].cpu().pin_memory() for k in ("q", "k", "v", "pos")}
@@ -393,20 +426,17 @@ class PromptCausal(Part):
         self.k_start, self.k_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         self.kernel_ms = []
 
-    def run(self, stream, host=None):
+    def calls(self, stream):
         s, c = SPEC[self.name], self.c
-        if host is not None:
-            for key in ("q", "k", "v"):
-                c[key].copy_(host[key], non_blocking=True)
-        self.k_start.record(stream)
         self.wa.prompt(c["q"], c["k"], c["v"], s["p0"], None, s["win"], 1.0, p32=s["p32"], out=self.out, ws=self.ws,
                        stream=stream)
-        self.k_end.record(stream)
-        if host is not None:
-            host["out"].copy_(self.out, non_blocking=True)
 
-    def collect(self):
-        self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
+    def copy_in(self, host):
+        for key in ("q", "k", "v"):
+            self.c[key].copy_(host[key], non_blocking=True)
+
+    def copy_out(self, host):
+        host["out"].copy_(self.out, non_blocking=True)
 
     def host_buffers(self):
         d = {k: self.c[k].cpu().pin_memory() for k in ("q", "k", "v")}
@@ -428,20 +458,17 @@ class PromptDense(Part):
         self.k_start, self.k_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         self.kernel_ms = []
 
-    def run(self, stream, host=None):
+    def calls(self, stream):
         s, c = SPEC[self.name], self.c
-        if host is not None:
-            c["qkv"].copy_(host["qkv"], non_blocking=True)
-            self.hi.copy_(host["hi"], non_blocking=True)
-        self.k_start.record(stream)
         self.wa.prompt(c["q"], c["k"], c["v"], 0, self.hi, 0, c["scale"], p32=s["p32"], out=self.out, ws=self.ws,
                        stream=stream)
-        self.k_end.record(stream)
-        if host is not None:
-            host["out"].copy_(self.out, non_blocking=True)
 
-    def collect(self):
-        self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
+    def copy_in(self, host):
+        self.c["qkv"].copy_(host["qkv"], non_blocking=True)
+        self.hi.copy_(host["hi"], non_blocking=True)
+
+    def copy_out(self, host):
+        host["out"].copy_(self.out, non_blocking=True)
 
     def host_buffers(self):
         return {"qkv": self.c["qkv"].cpu().pin_memory(), "hi": self.hi.cpu().pin_memory(),
@@ -466,17 +493,14 @@ class PrepDense(Part):
         self.k_start, self.k_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         self.kernel_ms = []
 
-    def run(self, stream, host=None):
-        if host is not None:
-            self.qkv.copy_(host["qkv"], non_blocking=True)
-        self.k_start.record(stream)
+    def calls(self, stream):
         self.wa.prep_append(self.qkv, self.pos, self.q, self.k, None, mode="rmsnorm", ws=self.ws, stream=stream)
-        self.k_end.record(stream)
-        if host is not None:
-            host["out"].copy_(self.qkv, non_blocking=True)
 
-    def collect(self):
-        self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
+    def copy_in(self, host):
+        self.qkv.copy_(host["qkv"], non_blocking=True)
+
+    def copy_out(self, host):
+        host["out"].copy_(self.qkv, non_blocking=True)
 
     def host_buffers(self):
         return {"qkv": self.qkv.cpu().pin_memory(), "out": torch_empty_pinned_like(self.qkv)}
@@ -497,21 +521,18 @@ class PromptSparse(Part):
         self.k_start, self.k_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         self.kernel_ms = []
 
-    def run(self, stream, host=None):
+    def calls(self, stream):
         s, c = SPEC[self.name], self.c
-        if host is not None:
-            for key in ("q", "k", "v"):
-                c[key].copy_(host[key], non_blocking=True)
-            self.sel.copy_(host["sel"], non_blocking=True)
-        self.k_start.record(stream)
         self.wa.prompt_sparse(c["q"], c["k"], c["v"], s["p0"], self.sel, None, s["win"], 1.0, p32=s["p32"],
                               out=self.out, ws=self.ws, stream=stream)
-        self.k_end.record(stream)
-        if host is not None:
-            host["out"].copy_(self.out, non_blocking=True)
 
-    def collect(self):
-        self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
+    def copy_in(self, host):
+        for key in ("q", "k", "v"):
+            self.c[key].copy_(host[key], non_blocking=True)
+        self.sel.copy_(host["sel"], non_blocking=True)
+
+    def copy_out(self, host):
+        host["out"].copy_(self.out, non_blocking=True)
 
     def host_buffers(self):
         d = {k: self.c[k].cpu().pin_memory() for k in ("q", "k", "v")}
@@ -814,8 +835,9 @@ def config_block(parts):
     return {"workload": " + ".join(parts), "parts": {p: SPEC[p] for p in parts},
             "l2": "inputs larger than L2 (each step streams > 40 GB of K/V and QKV); no flush",
             "peaks": "MEASURED_PEAKS.json hbm_gbs and bf16_tflops_sustained",
-            "launch": "multi-stream decode parts replay a CUDA graph of their calls; other parts call the C ABI "
-                      "eagerly; e2e calls everything eagerly with host copies"}
+            "launch": "each part's C-ABI calls replayed as a CUDA graph captured after one eager call (the "
+                      "three-stream parts fork and join inside the graph); e2e calls everything eagerly with "
+                      "host copies"}
 
 
 # ----------------------------------------------------------------------------- main
