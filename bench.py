@@ -556,13 +556,13 @@ PART_CLASSES = {"decode_sliding": DecodeSliding, "decode_linear": DecodeLinear,
 
 KERNEL_OF = {"decode_sliding": "decode partial (wa_decode.cu)", "decode_linear": "decode partial (wa_decode.cu)",
              "prompt_causal": "prompt tensor-core tile (wa_prompt_kernel.cuh)",
-             "prompt_dense": "prompt tensor-core tile (wa_prompt_kernel.cuh)",
+             "prompt_dense": "prompt tensor-core tiles, two query tiles a CTA (wa_prompt_pair.cuh)",
              "decode_gqa8": "tensor-core decode partial (wa_decode_tc.cu)",
              "decode_gqa16_linear": "tensor-core decode partial (wa_decode_tc.cu)",
              "prep_dense": "q/k preparation (wa_prep.cu)",
              "prompt_sparse": "block-sparse prompt tile (wa_prompt_sparse.cu)"}
 SOURCE_OF = {"decode_sliding": "wa_decode.cu", "decode_linear": "wa_decode.cu",
-             "prompt_causal": "wa_prompt_kernel.cuh", "prompt_dense": "wa_prompt_kernel.cuh",
+             "prompt_causal": "wa_prompt_kernel.cuh", "prompt_dense": "wa_prompt_pair.cuh",
              "decode_gqa8": "wa_decode_tc.cu", "decode_gqa16_linear": "wa_decode_tc.cu",
              "prep_dense": "wa_prep.cu", "prompt_sparse": "wa_prompt_kernel.cuh"}
 

@@ -1,9 +1,11 @@
 // wa_prompt.cu — prompt form (dense rows): instantiations, the tensor-map encoder, launches.
 //
-// The kernel is in wa_prompt_kernel.cuh; see there for the design and sources.
+// The kernels are in wa_prompt_kernel.cuh (head dim 256, and three P parts at 128) and
+// wa_prompt_pair.cuh (head dim 128 with one or two P parts); see there for the designs and sources.
 #include <mutex>
 
 #include "wa_prompt_kernel.cuh"
+#include "wa_prompt_pair.cuh"
 
 namespace wa {
 
@@ -23,8 +25,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 cudaError_t prompt_prepare_device(int) {
     cudaError_t e;
     if ((e = get_encoder()) != cudaSuccess) return e;
-    if ((e = set_attr<128, 1>()) != cudaSuccess) return e;
-    if ((e = set_attr<128, 2>()) != cudaSuccess) return e;
+    if ((e = set_pair_attr<1>()) != cudaSuccess) return e;
+    if ((e = set_pair_attr<2>()) != cudaSuccess) return e;
     if ((e = set_attr<128, 3>()) != cudaSuccess) return e;
     if ((e = set_attr<256, 1>()) != cudaSuccess) return e;
     if ((e = set_attr<256, 2>()) != cudaSuccess) return e;
@@ -38,7 +40,7 @@ cudaError_t launch_prompt(const PromptArgs& a, cudaStream_t s) {
         return a.p32 ? launch_t<256, 2, false>(a, s) : launch_t<256, 1, false>(a, s);
     }
     if (a.p32 == 2) return launch_t<128, 3, false>(a, s);
-    return a.p32 ? launch_t<128, 2, false>(a, s) : launch_t<128, 1, false>(a, s);
+    return a.p32 ? launch_pair<2>(a, s) : launch_pair<1>(a, s);
 }
 
 }  // namespace wa
