@@ -231,11 +231,12 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_pair_kernel(const __grid_c
                                     v0 + ((kk * 16 * 128) >> 4), idO, (tile > 0 || kk > 0 || part > 0) ? 1u : 0u);
                 mma_commit(BAR(PB_PVDONE + 2 * t + (tile & 1)));
             };
-            bool ok = mbar_wait(BAR(PB_Q), 0, p.status);
+            // The waits for K(j + 1) and V(j) come before the wait for P0(j): both are in shared
+            // memory long before the softmax of tile j is done, so once P0(j) is there nothing
+            // stands between O0 += P0(j) V(j) and S0(j + 1).
+            bool ok = mbar_wait(BAR(PB_Q), 0, p.status) && mbar_wait(BAR(PB_KFULL), 0, p.status);
             for (int j = 0; ok && j < ntiles; ++j) {
                 const int s = j & 1, u = j >> 1;
-                ok = mbar_wait(BAR(PB_KFULL + s), u & 1, p.status);
-                if (!ok) break;
                 tc_fence_after();
                 const uint64_t bk = sdesc_sw128(sbase + C::OFF_K + s * C::KV_BYTES, 16, 1024);
                 issue_s(0, j, aq0, bk);
@@ -246,8 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_pair_kernel(const __grid_c
                     issue_pv(1, j - 1);
                 }
                 issue_s(1, j, aq1, bk);
-                ok = mbar_wait(BAR(PB_PFULL + 0), j & 1, p.status);
-                if (ok) ok = mbar_wait(BAR(PB_VREADY + s), u & 1, p.status);
+                ok = mbar_wait(BAR(PB_VREADY + s), u & 1, p.status);
+                if (ok && j + 1 < ntiles) ok = mbar_wait(BAR(PB_KFULL + (s ^ 1)), ((j + 1) >> 1) & 1, p.status);
+                if (ok) ok = mbar_wait(BAR(PB_PFULL + 0), j & 1, p.status);
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(0, j);
