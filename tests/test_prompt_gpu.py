@@ -158,6 +158,32 @@ def test_chunk_split_gives_every_rows_bits(wa):
             assert torch.equal(both.view(torch.int16), whole.view(torch.int16)), (p32, cut)
 
 
+@pytest.mark.parametrize("p32", [False, True])
+def test_chunk_split_gives_every_rows_bits_d128(wa, p32):
+    """Head dim 128 (two 128-row query tiles a CTA): cuts on and off the 128- and 256-row tile
+    edges, with a window over a wrapping ring, give every row the bits of the whole chunk."""
+    n, p0, win, ring = 600, 1300, 700, 1400
+    c = _case(n, p0, 16, 8, 128, win, ring, seed=31, spans=[(500, 560)], outside="keep")
+    whole = wa.prompt(c["q"], c["k"], c["v"], p0, c["hi"], win, 1.0, p32=p32)
+    for cut in (1, 128, 255, 256, 301, 384, 499, 599):   # outside the image span (hi < p0 + cut)
+        a = wa.prompt(c["q"][:cut], c["k"], c["v"], p0, c["hi"][:cut].contiguous(), win, 1.0, p32=p32)
+        b = wa.prompt(c["q"][cut:], c["k"], c["v"], p0 + cut, c["hi"][cut:].contiguous(), win, 1.0, p32=p32)
+        both = torch.cat([a, b])
+        assert torch.equal(both.view(torch.int16), whole.view(torch.int16)), (p32, cut)
+
+
+def test_other_rows_do_not_change_a_rows_bits_d128(wa):
+    """A row's bits at head dim 128 depend on its own q and the keys it sees only: changing the
+    q of every other row (the tile that shares its CTA included) leaves them unchanged."""
+    n, p0 = 512, 0
+    c = _case(n, p0, 8, 2, 128, 0, 512, seed=32, outside="keep")
+    base = wa.prompt(c["q"], c["k"], c["v"], p0, None, 0, 1.0, p32=False)
+    keep = torch.arange(n, device="cuda") % 5 == 0
+    q2 = torch.where(keep[:, None, None], c["q"], -2 * c["q"])
+    out = wa.prompt(q2, c["k"], c["v"], p0, None, 0, 1.0, p32=False)
+    assert torch.equal(out[keep].view(torch.int16), base[keep].view(torch.int16))
+
+
 def test_linear_cache_declared_16x_longer_gives_same_bits(wa):
     c = _case(300, 0, 8, 4, 128, 0, 300, seed=12, outside="keep")
     a = wa.prompt(c["q"], c["k"], c["v"], 0, None, 0, 1.0, p32=True)
