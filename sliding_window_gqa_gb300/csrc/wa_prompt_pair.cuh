@@ -62,9 +62,10 @@ struct PairCfg {
 // A parity wait for phase k is only sound while phase k + 1 cannot have completed: S-done and
 // P.V-done are per stage, so the phase after the one the producer waits for (the tile two later)
 // needs the very load the producer has not issued yet.
+// PHALF[q]: P of the tile's first 64 keys is in tensor memory; PFULL[q]: all of P is.
 enum : int {
     PB_Q = 0, PB_KFULL = 1, PB_VFULL = 3, PB_VREADY = 5, PB_SFULL = 7, PB_PFULL = 11, PB_PVDONE = 13,
-    PB_DRAIN = 17
+    PB_DRAIN = 17, PB_PHALF = 18
 };
 
 template <int NP>
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_pair_kernel(const __grid_c
             mbar_init(BAR(PB_VFULL + s), 1);
             mbar_init(BAR(PB_VREADY + s), 1);
             mbar_init(BAR(PB_PFULL + s), 4);     // [q]: one arrival per softmax warp of the tile
+            mbar_init(BAR(PB_PHALF + s), 4);
         }
         for (int qs = 0; qs < 4; ++qs) {
             mbar_init(BAR(PB_SFULL + qs), 1);    // [q][s]: MMA commits
@@ -221,15 +223,31 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_pair_kernel(const __grid_c
                                 bk + (((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
                 mma_commit(BAR(PB_SFULL + 2 * t + (tile & 1)));
             };
-            auto issue_pv = [&](int t, int tile) {
+            // O(t) += P(t) V over the keys of one 64-key half of the tile (K steps 4 hh .. 4 hh + 3),
+            // every P part; the second half's products are followed by the P.V-done commit.
+            auto issue_pv_half = [&](int t, int tile, int hh) {
                 const uint64_t v0 = sdesc_sw128(sbase + C::OFF_V + (tile & 1) * C::KV_BYTES, C::KV_BLOCK, 1024);
 #pragma unroll
                 for (int part = 0; part < NP; ++part)
 #pragma unroll
-                    for (int kk = 0; kk < T / 16; ++kk)
-                        mma_bf16_ts(tbase + C::o_col(t), tbase + C::s_col(t) + (kk >> 2) * 64 + part * 32 + (kk & 3) * 8,
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const int kk = 4 * hh + k4;
+                        mma_bf16_ts(tbase + C::o_col(t), tbase + C::s_col(t) + hh * 64 + part * 32 + k4 * 8,
                                     v0 + ((kk * 16 * 128) >> 4), idO, (tile > 0 || kk > 0 || part > 0) ? 1u : 0u);
-                mma_commit(BAR(PB_PVDONE + 2 * t + (tile & 1)));
+                    }
+                if (hh == 1) mma_commit(BAR(PB_PVDONE + 2 * t + (tile & 1)));
+            };
+            // P.V of a tile in two halves: the first 64 keys' products start while the softmax
+            // still works on the second 64, which shortens each query tile's S -> softmax -> P.V
+            // chain by a half P.V.
+            auto issue_pv = [&](int t, int tile) -> bool {
+                if (!mbar_wait(BAR(PB_PHALF + t), tile & 1, p.status)) return false;
+                tc_fence_after();
+                issue_pv_half(t, tile, 0);
+                if (!mbar_wait(BAR(PB_PFULL + t), tile & 1, p.status)) return false;
+                tc_fence_after();
+                issue_pv_half(t, tile, 1);
+                return true;
             };
             // The waits for K(j + 1) and V(j) come before the wait for P0(j): both are in shared
             // memory long before the softmax of tile j is done, so once P0(j) is there nothing
@@ -240,27 +258,13 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_pair_kernel(const __grid_c
                 tc_fence_after();
                 const uint64_t bk = sdesc_sw128(sbase + C::OFF_K + s * C::KV_BYTES, 16, 1024);
                 issue_s(0, j, aq0, bk);
-                if (j >= 1) {
-                    ok = mbar_wait(BAR(PB_PFULL + 1), (j - 1) & 1, p.status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(1, j - 1);
-                }
+                if (j >= 1 && !(ok = issue_pv(1, j - 1))) break;
                 issue_s(1, j, aq1, bk);
                 ok = mbar_wait(BAR(PB_VREADY + s), u & 1, p.status);
                 if (ok && j + 1 < ntiles) ok = mbar_wait(BAR(PB_KFULL + (s ^ 1)), ((j + 1) >> 1) & 1, p.status);
-                if (ok) ok = mbar_wait(BAR(PB_PFULL + 0), j & 1, p.status);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(0, j);
+                if (ok) ok = issue_pv(0, j);
             }
-            if (ok) {
-                ok = mbar_wait(BAR(PB_PFULL + 1), (ntiles - 1) & 1, p.status);
-                if (ok) {
-                    tc_fence_after();
-                    issue_pv(1, ntiles - 1);
-                }
-            }
+            if (ok) ok = issue_pv(1, ntiles - 1);
             // every MMA issued so far has finished before tensor memory can be released
             mma_commit(BAR(PB_DRAIN));
             mbar_wait(BAR(PB_DRAIN), 0, p.status);
@@ -393,6 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_pair_kernel(const __grid_c
                     }
 #pragma unroll
                     for (int part = 0; part < NP; ++part) tmem_st16(t_s + half * 64 + part * 32 + cc * 16, w[part]);
+                }
+                if (half == 0) {   // the first half's P (and any O rescale above) is in place
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(PB_PHALF + q));
                 }
             }
             const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
