@@ -74,8 +74,8 @@ SPEC = {
 
 # ncu DRAM bytes per launch of the dominant kernels, valid only while the kernel source is unchanged.
 TRAFFIC = {
-    "prompt_dense": {"bytes_per_launch": 2057 * 10**6, "source_sha": "7e5dc4097ec6a1c3",
-                     "note": "ncu at N=8192 (353.1 MB read + 92.6 MB write), scaled by N to 37,810"},
+    "prompt_dense": {"bytes_per_launch": 2059 * 10**6, "source_sha": "f344a5021ad67644",
+                     "note": "ncu at N=8192 (352.5 MB read + 93.5 MB write), scaled by N to 37,810"},
     "decode_gqa8": {"bytes_per_launch": 853 * 10**6, "source_sha": "2033d7ed7d9eaec4",
                     "note": "the part's three launches together, like its achieved figure: ncu at 256 rows, one cache "
                             "(1.134 GB read + 8.0 MB write for 1.072 GB algorithmic), scaled by algorithmic bytes "
