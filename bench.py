@@ -930,7 +930,8 @@ def main():
         line["e2e"] = {"value": weak_scaling_value(t_roof, e2e["ms_per_step"], world), "unit": UNIT,
                        "h2d_bytes_per_step": e2e["h2d_bytes_per_step"], "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
                        "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"]}
-    if rank == 0 and not args.no_cpu_baseline:
+    # the oracle baseline is one host's figure: timed on rank 0 of a one-GPU run only
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t_cpu, desc = oracle_sample(parts, args.cpu_budget)
         line["cpu_baseline"] = {"value": t_roof / t_cpu, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                                 "sample": desc + "; extrapolated to the full workload by work"}
