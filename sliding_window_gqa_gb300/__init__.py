@@ -126,7 +126,76 @@ def prompt_ws_bytes(n: int, hq: int) -> int:
 def _workspace(nbytes: int, device, ws):
     if ws is None:
         return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda or ws.device != device or not ws.is_contiguous():
+        raise TypeError("ws must be a contiguous CUDA tensor on the inputs' device")
     return ws
+
+
+def _ws_bytes(ws) -> int:
+    return int(ws.numel() * ws.element_size())
+
+
+def _same_device(device, **ts) -> None:
+    for name, t in ts.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, the other inputs on {device}")
+
+
+# Shape agreement between the tensors of one call.  The C ABI receives bare pointers and
+# trusts these extents, so a mismatch here would become an out-of-bounds access there.
+
+def _decode_shapes(q, k_ring, v_ring, pos, out):
+    """(rows, hq, hkv, d, ring) of a decode call; ValueError if the tensors disagree."""
+    if q.dim() != 3 or k_ring.dim() != 4:
+        raise ValueError("q must be [rows, hq, d] and k_ring [rows, ring, hkv, d]")
+    rows, hq, d = q.shape
+    if k_ring.shape[0] != rows or k_ring.shape[3] != d:
+        raise ValueError(f"k_ring {tuple(k_ring.shape)} does not match q {tuple(q.shape)}")
+    if tuple(v_ring.shape) != tuple(k_ring.shape):
+        raise ValueError(f"v_ring {tuple(v_ring.shape)} must have k_ring's shape {tuple(k_ring.shape)}")
+    if pos.dim() != 1 or pos.numel() != rows or not pos.is_contiguous():
+        raise ValueError(f"pos must be a contiguous vector of {rows} positions")
+    if out is not None and (out.dtype != torch.bfloat16 or tuple(out.shape) != tuple(q.shape)
+                            or not out.is_contiguous()):
+        raise ValueError(f"out must be a contiguous bf16 tensor of q's shape {tuple(q.shape)}")
+    return rows, hq, k_ring.shape[2], d, k_ring.shape[1]
+
+
+def _prompt_shapes(q, k, v, hi, out):
+    """(n, hq, hkv, d, ring) of a prompt call; ValueError if the tensors disagree."""
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q must be [n, hq, d] and k, v [ring, hkv, d]")
+    n, hq, d = q.shape
+    ring, hkv, dk = k.shape
+    if dk != d:
+        raise ValueError(f"k's head dim {dk} differs from q's {d}")
+    if tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"v {tuple(v.shape)} must have k's shape {tuple(k.shape)}")
+    if hi is not None and (hi.dtype != torch.int32 or hi.dim() != 1 or hi.numel() != n or not hi.is_contiguous()):
+        raise TypeError("hi must be None or a contiguous int32 tensor of n elements")
+    if out is not None and (out.dtype != torch.bfloat16 or tuple(out.shape) != (n, hq, d)):
+        raise ValueError(f"out must be a bf16 tensor of shape {(n, hq, d)}")
+    return n, hq, hkv, d, ring
+
+
+def _prep_shapes(src, pos, q_out, k_ring, v_ring):
+    """(n, hq, hkv, d) of a preparation call; ValueError if the tensors disagree."""
+    if src.dim() != 2 or q_out.dim() != 3 or k_ring.dim() not in (3, 4):
+        raise ValueError("src must be [n, row], q_out [n, hq, d], k_ring [ring, hkv, d] or [n, ring, hkv, d]")
+    n = src.shape[0]
+    d = k_ring.shape[-1]
+    hq, hkv = q_out.shape[1], k_ring.shape[-2]
+    if q_out.shape[0] != n or q_out.shape[2] != d:
+        raise ValueError(f"q_out {tuple(q_out.shape)} does not match {n} tokens of head dim {d}")
+    if src.shape[1] < (hq + 2 * hkv) * d:
+        raise ValueError(f"src rows hold {src.shape[1]} values, fewer than (hq + 2 hkv) d = {(hq + 2 * hkv) * d}")
+    if k_ring.dim() == 4 and k_ring.shape[0] != n:
+        raise ValueError(f"per-token rings: k_ring has {k_ring.shape[0]} rings for {n} tokens")
+    if v_ring is not None and tuple(v_ring.shape) != tuple(k_ring.shape):
+        raise ValueError(f"v_ring {tuple(v_ring.shape)} must have k_ring's shape {tuple(k_ring.shape)}")
+    if pos.dim() != 1 or pos.numel() != n or not pos.is_contiguous():
+        raise ValueError(f"pos must be a contiguous vector of {n} positions")
+    return n, hq, hkv, d
 
 
 def decode(q, k_ring, v_ring, pos, win: int, scale: float = 1.0, out=None, ws=None, stream=None):
@@ -140,14 +209,15 @@ def decode(q, k_ring, v_ring, pos, win: int, scale: float = 1.0, out=None, ws=No
             raise ValueError(f"{n_} must be contiguous")
     if pos.dtype != torch.int32 or not pos.is_cuda:
         raise TypeError("pos must be an int32 CUDA tensor")
-    rows, hq, d = q.shape
-    _, ring, hkv, _ = k_ring.shape
+    rows, hq, hkv, d, ring = _decode_shapes(q, k_ring, v_ring, pos, out)
+    _same_device(q.device, k_ring=k_ring, v_ring=v_ring, pos=pos, out=out)
     if out is None:
         out = torch.empty_like(q)
     nbytes = decode_ws_bytes(rows, hq, d, win, ring)
     ws = _workspace(nbytes, q.device, ws)
     rc = lib().wa_decode(q.data_ptr(), k_ring.data_ptr(), v_ring.data_ptr(), pos.data_ptr(), rows, hq, hkv, d,
-                         win, ring, float(scale), out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream))
+                         win, ring, float(scale), out.data_ptr(), ws.data_ptr(), _ws_bytes(ws),
+                         _stream_handle(stream))
     if rc != WA_OK:
         raise WAError(rc, "wa_decode")
     return out
@@ -168,10 +238,8 @@ def prompt(q, k, v, p0: int, hi=None, win: int = 0, scale: float = 1.0, p32=Fals
     parts).  Returns out [n,hq,d] bf16."""
     for n_, t in (("q", q), ("k", k), ("v", v)):
         _check_bf16(n_, t)
-    n, hq, d = q.shape
-    ring, hkv, _ = k.shape
-    if hi is not None and (hi.dtype != torch.int32 or not hi.is_cuda or hi.numel() != n):
-        raise TypeError("hi must be None or an int32 CUDA tensor of n elements")
+    n, hq, hkv, d, ring = _prompt_shapes(q, k, v, hi, out)
+    _same_device(q.device, k=k, v=v, hi=hi, out=out)
     if out is None:
         out = torch.empty((n, hq, d), dtype=torch.bfloat16, device=q.device)
     st = _Strides(_token_stride("q", q, d), _token_stride("k", k, d), _token_stride("v", v, d),
@@ -179,7 +247,7 @@ def prompt(q, k, v, p0: int, hi=None, win: int = 0, scale: float = 1.0, p32=Fals
     ws = _workspace(prompt_ws_bytes(n, hq), q.device, ws)
     rc = lib().wa_prompt(q.data_ptr(), k.data_ptr(), v.data_ptr(), int(p0), n,
                          None if hi is None else hi.data_ptr(), hq, hkv, d, int(win), ring, float(scale),
-                         int(p32), ctypes.byref(st), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                         int(p32), ctypes.byref(st), out.data_ptr(), ws.data_ptr(), _ws_bytes(ws),
                          _stream_handle(stream))
     if rc != WA_OK:
         raise WAError(rc, "wa_prompt")
@@ -192,13 +260,11 @@ def prompt_sparse(q, k, v, p0: int, sel, hi=None, win: int = 0, scale: float = 1
     64-key blocks (-1 = unused).  Returns out [n,hq,d] bf16."""
     for n_, t in (("q", q), ("k", k), ("v", v)):
         _check_bf16(n_, t)
-    n, hq, d = q.shape
-    ring, hkv, _ = k.shape
-    if hi is not None and (hi.dtype != torch.int32 or not hi.is_cuda or hi.numel() != n):
-        raise TypeError("hi must be None or an int32 CUDA tensor of n elements")
+    n, hq, hkv, d, ring = _prompt_shapes(q, k, v, hi, out)
     if sel.dtype != torch.int32 or not sel.is_cuda or not sel.is_contiguous() or sel.dim() != 3 or \
             sel.shape[0] != n or sel.shape[1] != hkv:
         raise TypeError("sel must be a contiguous int32 CUDA tensor [n, hkv, nsel]")
+    _same_device(q.device, k=k, v=v, hi=hi, sel=sel, out=out)
     if out is None:
         out = torch.empty((n, hq, d), dtype=torch.bfloat16, device=q.device)
     st = _Strides(_token_stride("q", q, d), _token_stride("k", k, d), _token_stride("v", v, d),
@@ -207,7 +273,7 @@ def prompt_sparse(q, k, v, p0: int, sel, hi=None, win: int = 0, scale: float = 1
     rc = lib().wa_prompt_sparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), int(p0), n,
                                 None if hi is None else hi.data_ptr(), hq, hkv, d, int(win), ring, float(scale),
                                 int(p32), sel.data_ptr(), sel.shape[2], ctypes.byref(st), out.data_ptr(),
-                                ws.data_ptr(), ws.numel(), _stream_handle(stream))
+                                ws.data_ptr(), _ws_bytes(ws), _stream_handle(stream))
     if rc != WA_OK:
         raise WAError(rc, "wa_prompt_sparse")
     return out
@@ -245,9 +311,8 @@ def prep_append(src, pos, q_out, k_ring, v_ring=None, mode: str = "rmsnorm", q_s
         raise TypeError("pos must be an int32 CUDA tensor")
     if src.dim() != 2 or src.stride(1) != 1:
         raise ValueError("src must be [n, row] with unit inner stride")
-    n = src.shape[0]
-    d = k_ring.shape[-1]
-    hq, hkv = q_out.shape[1], k_ring.shape[-2]
+    n, hq, hkv, d = _prep_shapes(src, pos, q_out, k_ring, v_ring)
+    _same_device(src.device, pos=pos, q_out=q_out, k_ring=k_ring, v_ring=v_ring, q_scale=q_scale, inv_freq=inv_freq)
     ring, ring_row, slot = _ring_layout("k_ring", k_ring, d)
     if v_ring is not None and _ring_layout("v_ring", v_ring, d) != (ring, ring_row, slot):
         raise ValueError("v_ring must have k_ring's layout")
@@ -260,7 +325,7 @@ def prep_append(src, pos, q_out, k_ring, v_ring=None, mode: str = "rmsnorm", q_s
                               None if q_scale is None else q_scale.data_ptr(),
                               None if inv_freq is None else inv_freq.data_ptr(), ring, ctypes.byref(lay),
                               q_out.data_ptr(), k_ring.data_ptr(), None if v_ring is None else v_ring.data_ptr(),
-                              ws.data_ptr(), ws.numel(), _stream_handle(stream))
+                              ws.data_ptr(), _ws_bytes(ws), _stream_handle(stream))
     if rc != WA_OK:
         raise WAError(rc, "wa_prep_append")
     return ws
