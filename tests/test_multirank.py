@@ -40,7 +40,8 @@ def _worker(rank, world, port, results):
 
 def test_reduce_max_over_two_gloo_ranks():
     world = 2
-    with mp.Manager() as m:
+    # the result store is started by spawn, like the ranks: a fork of a threaded process can deadlock
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_worker, args=(world, _free_port(), results), nprocs=world, join=True)
         assert dict(results) == {0: 15.0, 1: 15.0}
