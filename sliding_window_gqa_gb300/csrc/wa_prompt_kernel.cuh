@@ -71,6 +71,7 @@ struct PromptParams {
     const int32_t* sel;   // [n, hkv, nsel] selected 64-key blocks, -1 = unused
     int nsel;
     int gsz;              // query heads per CTA row: lane m = (row m / gsz, head m % gsz); 1 for dense
+    int hfirst;           // CTAs in launch order take every head of one query tile before the next tile
 };
 
 constexpr int kSelMax = 64;        // block-sparse: selected blocks per row at most
@@ -282,14 +283,23 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
     float* xbuf = reinterpret_cast<float*>(smem + C::OFF_X);            // [2][2][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = p.nqt - 1 - static_cast<int>(blockIdx.x);            // longest (causal) tiles first
+    // CTA -> (query tile, head).  Tiles run longest (causal) first; with hfirst the launch order
+    // (x fastest, then y) takes every head of a tile before the next, so the longest CTAs of all
+    // heads start first instead of the last head's longest ones starting late.
+    int bx = static_cast<int>(blockIdx.x), by = static_cast<int>(blockIdx.y);
+    if (p.hfirst) {
+        const int lin = bx + by * static_cast<int>(gridDim.x);
+        bx = lin / static_cast<int>(gridDim.y);
+        by = lin % static_cast<int>(gridDim.y);
+    }
+    const int qt = p.nqt - 1 - bx;
     const int G = p.hq / p.hkv;
     // Dense: one query head, 128 rows, lane = row.  Block-sparse: the key head's G query heads
     // for R = 128 / G rows, lane m = (row m / G, head m % G).
     const int gsz = SP ? p.gsz : 1;
     const int nrows = kBM / gsz;
-    const int g = SP ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y) / G;
-    const int h0 = SP ? g * G : static_cast<int>(blockIdx.y);
+    const int g = SP ? by : by / G;
+    const int h0 = SP ? g * G : by;
     const int m0 = qt * nrows;
     uint32_t* bmap = reinterpret_cast<uint32_t*>(smem + C::OFF_BMAP);
     uint16_t* sel_lists = reinterpret_cast<uint16_t*>(smem + C::OFF_SEL);
@@ -766,6 +776,8 @@ cudaError_t launch_t(const PromptArgs& a, cudaStream_t s) {
     pp.sel = a.sel;
     pp.nsel = a.nsel;
     pp.gsz = gsz;
+    // causal on a linear cache: CTA lengths grow with the tile, so all heads' longest go first
+    pp.hfirst = (!SP && a.win == 0 && a.hi == nullptr) ? 1 : 0;
     const dim3 grid(pp.nqt, SP ? a.hkv : a.hq);
     prompt_kernel<D, NP, SP><<<grid, kThreads, C::SMEM, s>>>(pp);
     return cudaGetLastError();
