@@ -104,11 +104,14 @@ int wa_decode(const void* q, const void* k_ring, const void* v_ring, const int32
  *
  * The first call on each device looks up the array's device address (once,
  * with that device current); make that first call before any stream capture.
- * Every call on a device shares the one array, and each call clears the
- * status word and re-run counter at its start: calls whose work can overlap
- * on the GPU (for example, calls on two streams with no ordering between
- * them) race on it and must be ordered by the caller; calls on one stream are
- * ordered already.  The status word is not readable through wa_status.
+ * The address is kept for the life of the process: do not call this entry
+ * point again after cudaDeviceReset, which unloads the module that holds the
+ * array.  Every call on a device shares the one array, and each call clears
+ * the status word and re-run counter at its start: calls whose work can
+ * overlap on the GPU (for example, calls on two streams with no ordering
+ * between them) race on it and must be ordered by the caller; calls on one
+ * stream are ordered already.  wa_status(NULL, stream) returns the status
+ * bits the last call on the current device left in the array.
  */
 int wa_decode_static(const void* q, const void* k_ring, const void* v_ring, const int32_t* pos,
                      int32_t rows, int32_t hq, int32_t hkv, int32_t d, int32_t win, int32_t ring,
@@ -224,7 +227,9 @@ int wa_prep_append(const void* src, const int32_t* pos, int32_t n, int32_t hq, i
                    void* ws, size_t ws_bytes, void* stream);
 
 /* Waits for `stream`, then returns the WA_STATUS_* bits the last call that
- * used `ws` left (0 when clean), or a negative WA_E* code if the read fails. */
+ * used `ws` left (0 when clean), or a negative WA_E* code if the read fails.
+ * With ws NULL it reads the header of wa_decode_static's scratch array on the
+ * current device, i.e. the bits of the last wa_decode_static call there. */
 int wa_status(const void* ws, void* stream);
 
 /* Static description of a WA_* return code or WA_STATUS_* bit set. */

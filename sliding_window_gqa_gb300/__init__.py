@@ -17,7 +17,8 @@ import re
 import torch
 
 __all__ = [
-    "WAError", "lib", "lib_path", "decode", "prompt", "prompt_sparse", "prep_append", "status", "decode_ws_bytes", "prompt_ws_bytes",
+    "WAError", "lib", "lib_path", "decode", "decode_static", "prompt", "prompt_sparse", "prep_append", "status",
+    "decode_ws_bytes", "prompt_ws_bytes",
     "WA_OK", "WA_EINVAL", "WA_EWORKSPACE", "WA_ECUDA", "WA_EDEVICE",
     "WA_STATUS_BAD_POS", "WA_STATUS_BAD_HI", "WA_STATUS_TIMEOUT",
 ]
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.wa_decode_ws_bytes.restype = ctypes.c_size_t
         L.wa_decode.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, ctypes.c_size_t, _P]
         L.wa_decode.restype = ctypes.c_int
+        L.wa_decode_static.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P]
+        L.wa_decode_static.restype = ctypes.c_int
         L.wa_prompt_ws_bytes.argtypes = [_I, _I]
         L.wa_prompt_ws_bytes.restype = ctypes.c_size_t
         L.wa_prompt.argtypes = [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, ctypes.c_float, _I,
@@ -223,6 +226,28 @@ def decode(q, k_ring, v_ring, pos, win: int, scale: float = 1.0, out=None, ws=No
     return out
 
 
+def decode_static(q, k_ring, v_ring, pos, win: int, scale: float = 1.0, out=None, stream=None):
+    """decode() without a workspace: the library's fixed device scratch (WA_STATIC_WS_BYTES a
+    device) holds the partials, for callers that cannot allocate device memory.  Calls that
+    may overlap on the GPU share that scratch and must be ordered by the caller; the status
+    bits of the last call are status(None)."""
+    for n_, t in (("q", q), ("k_ring", k_ring), ("v_ring", v_ring)):
+        _check_bf16(n_, t)
+        if not t.is_contiguous():
+            raise ValueError(f"{n_} must be contiguous")
+    if pos.dtype != torch.int32 or not pos.is_cuda:
+        raise TypeError("pos must be an int32 CUDA tensor")
+    rows, hq, hkv, d, ring = _decode_shapes(q, k_ring, v_ring, pos, out)
+    _same_device(q.device, k_ring=k_ring, v_ring=v_ring, pos=pos, out=out)
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib().wa_decode_static(q.data_ptr(), k_ring.data_ptr(), v_ring.data_ptr(), pos.data_ptr(), rows, hq, hkv,
+                                d, win, ring, float(scale), out.data_ptr(), _stream_handle(stream))
+    if rc != WA_OK:
+        raise WAError(rc, "wa_decode_static")
+    return out
+
+
 def _token_stride(name: str, t: torch.Tensor, d: int) -> int:
     if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != d:
         raise ValueError(f"{name} must be [tokens, heads, d] with head stride d and unit dim stride")
@@ -332,8 +357,9 @@ def prep_append(src, pos, q_out, k_ring, v_ring=None, mode: str = "rmsnorm", q_s
 
 
 def status(ws, stream=None) -> int:
-    """WA_STATUS_* bits of the last call on ``ws`` (waits for the stream)."""
-    rc = lib().wa_status(ws.data_ptr(), _stream_handle(stream))
+    """WA_STATUS_* bits of the last call on ``ws`` (waits for the stream); ``ws`` None reads those
+    of the last decode_static call on the current device."""
+    rc = lib().wa_status(None if ws is None else ws.data_ptr(), _stream_handle(stream))
     if rc < 0:
         raise WAError(rc, "wa_status")
     return rc

@@ -226,7 +226,12 @@ int wa_prep_append(const void* src, const int32_t* pos, int32_t n, int32_t hq, i
 }
 
 int wa_status(const void* ws, void* stream) {
-    if (!ws) return WA_EWORKSPACE;
+    if (!ws) {   // the header of wa_decode_static's scratch on the current device
+        void* sws = nullptr;
+        const int rc = wa::static_ws_header(&sws);
+        if (rc != WA_OK) return rc;
+        ws = sws;
+    }
     int st = 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(&st, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return WA_ECUDA;

@@ -99,5 +99,7 @@ cudaError_t decode_prepare_device(int dev);
 constexpr int kTcMinGroup = 3;
 cudaError_t launch_decode_tc_part(const DecodeArgs& a, cudaStream_t s);
 cudaError_t decode_tc_prepare_device(int dev);
+// Device address of wa_decode_static's scratch on the current device (WA_OK or a WA_E* code).
+int static_ws_header(void** out);
 
 }  // namespace wa

@@ -63,6 +63,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+namespace wa {
+
+// The device address of the current device's static array (set up on first use), for wa_status
+// with a null workspace: its first 256 bytes are the header the last wa_decode_static call wrote.
+int static_ws_header(void** out) { return static_ws(out); }
+
+}  // namespace wa
+
 extern "C" int wa_decode_static(const void* q, const void* k_ring, const void* v_ring, const int32_t* pos,
                                 int32_t rows, int32_t hq, int32_t hkv, int32_t d, int32_t win, int32_t ring,
                                 float scale, void* out, void* stream) {
