@@ -11,22 +11,26 @@ Numerical Contract" page, "Canonical Boundary"):
   prompt_causal   8,192 rows at p0 0, 16/8 heads, d 256, linear cache, causal, P32
   prompt_dense    37,810 rows, 56 heads (MHA), d 128, interleaved QKV (row 21,504),
                   RMSNormed Q/K, scale 1/sqrt(128), non-causal (hi = N-1), bf16 P
+  prompt_dense_p32  the same workload with P as two bf16 parts (the page leaves the
+                  dense workload's P precision open, so it is timed both ways)
 
-Two more decode parts run only when named with --parts (they are not in the
-default step): decode_gqa8 (decode_sliding with 32 query heads over 4 key
-heads) and decode_gqa16_linear (decode_linear with 32 over 2), the groups the
-tensor-core decode serves.  prep_dense (optional too) is the dense workload's
-q/k preparation: per-head RMSNorm of Q and K in place in the interleaved QKV
-buffer (37,810 tokens, 56 heads, d 128), HBM-bound.  prompt_sparse (optional)
-is the block-sparse prompt of TensorFold #1622's shapes: 7,936 causal rows, 24/2
-heads, d 256, each row's 2,048 selected keys as 32 blocks of 64, three-part P;
-its flops count the visible selected keys only.
+The "next" parts run after the step, each timed the same way but outside the
+step and its value (they are not the headline workloads): decode_gqa8
+(decode_sliding with 32 query heads over 4 key heads) and decode_gqa16_linear
+(decode_linear with 32 over 2), the groups the tensor-core decode serves;
+prep_dense, the dense workload's q/k preparation (per-head RMSNorm of Q and K in
+place in the interleaved QKV buffer, 37,810 tokens, 56 heads, d 128), HBM-bound;
+and prompt_sparse, the block-sparse prompt of TensorFold #1622's shapes: 7,936
+causal rows, 24/2 heads, d 256, each row's 2,048 selected keys as 32 blocks of 64,
+three-part P, whose flops count the visible selected keys only.  --next none
+skips them.
 
 value = (decode bytes / HBM peak + prompt flops / bf16 peak) / measured step time:
 the step's roofline time over its measured time.  Decode bytes are the visible
 K and V rows plus q and out; prompt flops are 4*d per visible (row, key, head).
-Peaks come from MEASURED_PEAKS.json (the sustained bf16 figure, since each
-kernel runs inside a long step).
+Peaks come from MEASURED_PEAKS.json: the copy bandwidth and the burst bf16
+figure, since each part is timed alone by CUDA events around its own calls (the
+sustained figure is reported beside it).
 
 Each part's calls are captured once in a CUDA graph and replayed in the timed region (the
 three-stream parts fork and join inside it), as a serving loop would; the e2e leg calls the C
@@ -57,7 +61,7 @@ UNIT = "fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL_HBM_GBS = 8000.0   # the ~8 TB/s nominal figure, printed beside the measured-copy fraction
 
-PARTS = ("decode_sliding", "decode_linear", "prompt_causal", "prompt_dense")
+PARTS = ("decode_sliding", "decode_linear", "prompt_causal", "prompt_dense", "prompt_dense_p32")
 EXTRA_PARTS = ("decode_gqa8", "decode_gqa16_linear", "prep_dense", "prompt_sparse")
 SPEC = {
     "decode_sliding": dict(caches=3, rows=64, hq=32, hkv=16, d=256, win=1024, ring=1536, pos_max=40000,
@@ -65,6 +69,7 @@ SPEC = {
     "decode_linear": dict(rows=64, hq=32, hkv=16, d=256, win=0, ring=32768, seed=20260004),
     "prompt_causal": dict(n=8192, p0=0, hq=16, hkv=8, d=256, win=0, ring=8192, p32=True, seed=20260005),
     "prompt_dense": dict(N=37810, H=56, d=128, p32=False, seed=20260006),
+    "prompt_dense_p32": dict(N=37810, H=56, d=128, p32=True, seed=20260006),
     "decode_gqa8": dict(caches=3, rows=64, hq=32, hkv=4, d=256, win=1024, ring=1536, pos_max=40000,
                         seed=20260007),
     "decode_gqa16_linear": dict(rows=64, hq=32, hkv=2, d=256, win=0, ring=32768, seed=20260008),
@@ -181,10 +186,12 @@ def peaks():
 
 
 def roofline_seconds(parts, pk) -> float:
+    """Seconds the parts' algorithmic work takes at the peaks: bytes at the copy bandwidth, flops at
+    the burst bf16 rate (each part is timed alone, by CUDA events around its own calls)."""
     t = 0.0
     for part in parts:
         w = part_work(part)
-        t += w["bytes"] / (pk["hbm_gbs"] * 1e9) + w["flops"] / (pk["bf16_tflops_sustained"] * 1e12)
+        t += w["bytes"] / (pk["hbm_gbs"] * 1e9) + w["flops"] / (pk["bf16_tflops"] * 1e12)
     return t
 
 
@@ -541,6 +548,10 @@ class PromptSparse(Part):
         return d
 
 
+class PromptDenseP32(PromptDense):
+    name = "prompt_dense_p32"
+
+
 class DecodeGqa8(DecodeSliding):
     name = "decode_gqa8"
 
@@ -550,19 +561,21 @@ class DecodeGqa16Linear(DecodeLinear):
 
 
 PART_CLASSES = {"decode_sliding": DecodeSliding, "decode_linear": DecodeLinear,
-                "prompt_causal": PromptCausal, "prompt_dense": PromptDense,
+                "prompt_causal": PromptCausal, "prompt_dense": PromptDense, "prompt_dense_p32": PromptDenseP32,
                 "decode_gqa8": DecodeGqa8, "decode_gqa16_linear": DecodeGqa16Linear, "prep_dense": PrepDense,
                 "prompt_sparse": PromptSparse}
 
 KERNEL_OF = {"decode_sliding": "decode partial (wa_decode.cu)", "decode_linear": "decode partial (wa_decode.cu)",
              "prompt_causal": "prompt tensor-core tile (wa_prompt_kernel.cuh)",
              "prompt_dense": "prompt tensor-core tiles, two query tiles a CTA (wa_prompt_pair.cuh)",
+             "prompt_dense_p32": "prompt tensor-core tiles, two query tiles a CTA, two P parts (wa_prompt_pair.cuh)",
              "decode_gqa8": "tensor-core decode partial (wa_decode_tc.cu)",
              "decode_gqa16_linear": "tensor-core decode partial (wa_decode_tc.cu)",
              "prep_dense": "q/k preparation (wa_prep.cu)",
              "prompt_sparse": "block-sparse prompt tile (wa_prompt_sparse.cu)"}
 SOURCE_OF = {"decode_sliding": "wa_decode.cu", "decode_linear": "wa_decode.cu",
              "prompt_causal": "wa_prompt_kernel.cuh", "prompt_dense": "wa_prompt_pair.cuh",
+             "prompt_dense_p32": "wa_prompt_pair.cuh",
              "decode_gqa8": "wa_decode_tc.cu", "decode_gqa16_linear": "wa_decode_tc.cu",
              "prep_dense": "wa_prep.cu", "prompt_sparse": "wa_prompt_kernel.cuh"}
 
@@ -669,7 +682,33 @@ def run_native(args, parts, rank, world, dist):
         del host
     per_part_ms = {o.name: statistics.median(o.kernel_ms) for o in objs}
     launches = sum(o.launches for o in objs) * args.steps
-    return ms_per_step, per_part_ms, clk, e2e, launches
+    del objs
+    nxt = time_next_parts(args, torch, wa, wa_synth, dev, stream) if args.next_parts else None
+    return ms_per_step, per_part_ms, clk, e2e, launches, nxt
+
+
+def time_next_parts(args, torch, wa, wa_synth, dev, stream):
+    """The "next" parts, one after another: W warm-up calls, then K calls each timed by CUDA events
+    on the launching stream (graph replays, as in the step), with clocks sampled meanwhile."""
+    out = {}
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    for name in args.next_parts:
+        o = PART_CLASSES[name](torch, wa, wa_synth, dev)
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            o.run(stream)
+        torch.cuda.synchronize()
+        o.kernel_ms = []
+        for _ in range(args.steps):
+            o.run(stream)
+            torch.cuda.synchronize()
+            o.collect()
+        out[name] = {"ms": statistics.median(o.kernel_ms), "launches": o.launches * args.steps}
+        del o
+        torch.cuda.empty_cache()
+    out["clocks"] = clocks.stop()
+    return out
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
@@ -798,6 +837,47 @@ def oracle_sample(parts, budget_s: float):
     return total, "; ".join(desc)
 
 
+def report_part(p: str, ms: float, pk) -> dict:
+    """A part's time with its algorithmic throughput and fractions of the peaks."""
+    w = part_work(p)
+    if w["bytes"]:
+        gbs = w["bytes"] / (ms * 1e-3) / 1e9
+        return {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm_gbs"],
+                "frac_hbm_nominal_8tbs": gbs / NOMINAL_HBM_GBS, "bytes": w["bytes"]}
+    tf = w["flops"] / (ms * 1e-3) / 1e12
+    return {"ms": ms, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops"],
+            "frac_bf16_sustained": tf / pk["bf16_tflops_sustained"],
+            "flops": w["flops"], "issued_TFLOP/s": tf * w.get("issued_flops_factor", 1.0)}
+
+
+def oracle_one_core(parts, budget_s: float):
+    """The oracle sample again in a child process pinned to one core, with every math library held to
+    one thread (the variables must be set before numpy loads).  None if the child fails."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[var] = "1"
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-one-core", "--cpu-budget", str(budget_s),
+           "--parts", ",".join(parts), "--no-next"]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=60 + 20 * budget_s)
+    except subprocess.TimeoutExpired:
+        return None
+    if r.returncode != 0 or not r.stdout.strip():
+        return None
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def run_oracle_one_core(args, parts):
+    """Child side of oracle_one_core: pin to the first allowed core, time the sample, print JSON."""
+    try:
+        cpus = sorted(os.sched_getaffinity(0))
+        os.sched_setaffinity(0, {cpus[0]})
+    except (AttributeError, OSError):
+        pass
+    t, desc = oracle_sample(parts, args.cpu_budget)
+    print(json.dumps({"seconds": t, "sample": desc}), flush=True)
+
+
 def cpu_threads() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -834,7 +914,7 @@ def run_reference(args, parts):
 def config_block(parts):
     return {"workload": " + ".join(parts), "parts": {p: SPEC[p] for p in parts},
             "l2": "inputs larger than L2 (each step streams > 40 GB of K/V and QKV); no flush",
-            "peaks": "MEASURED_PEAKS.json hbm_gbs and bf16_tflops_sustained",
+            "peaks": "MEASURED_PEAKS.json hbm_gbs and bf16_tflops (burst; each part is timed alone)",
             "launch": "each part's C-ABI calls replayed as a CUDA graph captured after one eager call (the "
                       "three-stream parts fork and join inside the graph); e2e calls everything eagerly with "
                       "host copies"}
@@ -849,20 +929,24 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--parts", default="all", help="comma list of " + ",".join(PARTS + EXTRA_PARTS))
+    ap.add_argument("--next", default="all", help="comma list of the parts timed after the step: "
+                    + ",".join(EXTRA_PARTS) + ", or none")
+    ap.add_argument("--no-next", action="store_true", help="same as --next none")
+    ap.add_argument("--oracle-one-core", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=4.0, help="oracle seconds per reference step")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="oracle seconds for cpu_baseline")
     ap.add_argument("--caches", type=int, default=None, help="override the decode_sliding cache count (profiling)")
-    ap.add_argument("--dense-n", type=int, default=None, help="override the prompt_dense and prep_dense row count (profiling)")
+    ap.add_argument("--dense-n", type=int, default=None, help="override the dense prompts' and prep_dense's row count (profiling)")
     ap.add_argument("--decode-rows", type=int, default=None, help="override every decode part's rows per cache (profiling)")
     args = ap.parse_args()
     if args.caches is not None:
         SPEC["decode_sliding"]["caches"] = args.caches
     if args.dense_n is not None:
-        SPEC["prompt_dense"]["N"] = args.dense_n
-        SPEC["prep_dense"]["N"] = args.dense_n
+        for name in ("prompt_dense", "prompt_dense_p32", "prep_dense"):
+            SPEC[name]["N"] = args.dense_n
     if args.decode_rows is not None:
         for name, sp in SPEC.items():
             if name.startswith("decode"):
@@ -872,6 +956,17 @@ def main():
     for p in parts:
         if p not in PARTS and p not in EXTRA_PARTS:
             raise SystemExit(f"unknown part {p}")
+    if args.no_next or args.next == "none":
+        args.next_parts = []
+    else:
+        args.next_parts = [p for p in (EXTRA_PARTS if args.next == "all" else args.next.split(",")) if p
+                           and p not in parts]
+    for p in args.next_parts:
+        if p not in EXTRA_PARTS:
+            raise SystemExit(f"unknown next part {p}")
+    if args.oracle_one_core:
+        run_oracle_one_core(args, parts)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -882,29 +977,18 @@ def main():
 
     dist = None
     if world > 1:
+        args.next_parts = []   # the next parts are a one-GPU report
         import torch
         import torch.distributed as tdist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         tdist.init_process_group("nccl")
         dist = tdist
-    ms_per_step, per_part_ms, clk, e2e, launches = run_native(args, parts, rank, world, dist)
+    ms_per_step, per_part_ms, clk, e2e, launches, nxt = run_native(args, parts, rank, world, dist)
     pk = peaks()
     t_roof = roofline_seconds(parts, pk)
     value = weak_scaling_value(t_roof, ms_per_step, world)
 
-    part_report = {}
-    for p in parts:
-        w = part_work(p)
-        ms = per_part_ms[p]
-        if w["bytes"]:
-            gbs = w["bytes"] / (ms * 1e-3) / 1e9
-            part_report[p] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / pk["hbm_gbs"],
-                              "frac_hbm_nominal_8tbs": gbs / NOMINAL_HBM_GBS, "bytes": w["bytes"]}
-        else:
-            tf = w["flops"] / (ms * 1e-3) / 1e12
-            part_report[p] = {"ms": ms, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops_sustained"],
-                              "frac_bf16_burst": tf / pk["bf16_tflops"],
-                              "flops": w["flops"], "issued_TFLOP/s": tf * w.get("issued_flops_factor", 1.0)}
+    part_report = {p: report_part(p, per_part_ms[p], pk) for p in parts}
     dom = max(parts, key=lambda p: per_part_ms[p])
     w = part_work(dom)
     ms = per_part_ms[dom]
@@ -913,12 +997,14 @@ def main():
         roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"]}
     else:
         ach = w["flops"] / (ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": ach / pk["bf16_tflops_sustained"]}
+        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_tflops"], "peak_sustained": pk["bf16_tflops_sustained"],
+                "frac_sustained": ach / pk["bf16_tflops_sustained"]}
     tr = TRAFFIC.get(dom)
     roof["traffic"] = tr["bytes_per_launch"] if tr and tr.get("source_sha") == source_hash(SOURCE_OF[dom]) else None
     roof["kernel"] = KERNEL_OF[dom] + f", part {dom}; per-launch time from CUDA events around the C-ABI call"
-    roof["peak_source"] = pk["source"] + (" (sustained bf16)" if roof["bound"] == "tensor" else " (copy GB/s)")
+    roof["peak_source"] = pk["source"] + (" (burst bf16; the part is timed alone)" if roof["bound"] == "tensor"
+                                          else " (copy GB/s)")
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -926,6 +1012,11 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_block(parts),
         "parts": part_report, "roofline": roof, "clocks": clk, "gpu_launches": launches,
     }
+    if nxt is not None:
+        line["next_parts"] = {p: report_part(p, nxt[p]["ms"], pk) for p in args.next_parts}
+        line["next_parts"]["clocks"] = nxt["clocks"]
+        line["next_parts"]["note"] = ("timed after the step, outside its value; each part's graph replay "
+                                      "timed by CUDA events, median of the steps")
     if e2e is not None:
         line["e2e"] = {"value": weak_scaling_value(t_roof, e2e["ms_per_step"], world), "unit": UNIT,
                        "h2d_bytes_per_step": e2e["h2d_bytes_per_step"], "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
@@ -935,6 +1026,10 @@ def main():
         t_cpu, desc = oracle_sample(parts, args.cpu_budget)
         line["cpu_baseline"] = {"value": t_roof / t_cpu, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                                 "sample": desc + "; extrapolated to the full workload by work"}
+        one = oracle_one_core(parts, args.cpu_budget / 2)
+        if one is not None:
+            line["cpu_baseline"]["one_core"] = {"value": t_roof / one["seconds"], "cores": 1,
+                                                "sample": one["sample"] + "; extrapolated to the full workload by work"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

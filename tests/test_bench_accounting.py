@@ -67,7 +67,26 @@ def test_prep_bytes_and_weak_scaling():
 
 
 def test_roofline_seconds_adds_bytes_and_flops():
-    pk = {"hbm_gbs": 1000.0, "bf16_tflops_sustained": 1000.0}
+    """Bytes at the copy bandwidth, flops at the burst bf16 rate (each part is timed alone)."""
+    pk = {"hbm_gbs": 1000.0, "bf16_tflops": 1000.0, "bf16_tflops_sustained": 500.0}
     t = bench.roofline_seconds(["decode_linear", "prompt_dense"], pk)
     w1, w2 = bench.part_work("decode_linear"), bench.part_work("prompt_dense")
     assert np.isclose(t, w1["bytes"] / 1e12 + w2["flops"] / 1e15)
+
+
+def test_dense_workload_is_timed_in_both_p_modes():
+    """The dense workload's P precision is open, so the step holds it with one and with two P parts;
+    both count the same algorithmic flops (the second part's products are issued, not algorithmic)."""
+    assert "prompt_dense" in bench.PARTS and "prompt_dense_p32" in bench.PARTS
+    a, b = bench.part_work("prompt_dense"), bench.part_work("prompt_dense_p32")
+    assert a["flops"] == b["flops"]
+    assert a["issued_flops_factor"] == 1.0 and b["issued_flops_factor"] == 1.5
+
+
+def test_part_report_fractions_use_the_burst_peak():
+    pk = {"hbm_gbs": 1000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}
+    w = bench.part_work("prompt_causal")
+    ms = w["flops"] / 1e12 / 1000.0 * 1e3          # 1,000 TFLOP/s
+    r = bench.report_part("prompt_causal", ms, pk)
+    assert np.isclose(r["TFLOP/s"], 1000.0)
+    assert np.isclose(r["frac_bf16"], 0.5) and np.isclose(r["frac_bf16_sustained"], 0.625)
