@@ -9,11 +9,21 @@
 // in its selected 64-key blocks (TensorFold pull request #1622); a row with none
 // gets 0 / 0 = NaN, as the formula's empty sums give.
 //
-// One CTA takes one flagged (row, head) at a time.  Pass 1 finds the
-// NaN-propagating maximum score; pass 2 forms w_j = exp(s_j - M) block by
-// block and accumulates sum_j w_j v_j in key order, one thread per output
-// dim.  Key j always goes to thread (j - lo) mod 256 and the reductions use
-// fixed trees, so the bits depend only on the row's own inputs.
+// A grid of a few CTAs per SM (at most one per (row, head)) walks the flagged
+// list; with nothing flagged every CTA exits at once.  Per flagged head:
+//   pass 0  fp32 scores (each bf16 x bf16 product is exact in fp32), keys in
+//           parallel, 256 at a time.  A key whose fp32 score is not finite is
+//           scored again in float64; a float64 score that is NaN or +inf makes
+//           the NaN-propagating maximum M NaN or +inf, and then every weight
+//           exp(s_j - M) of the formula is NaN or 0 with a NaN sum: the output
+//           is NaN, written at once without the float64 passes.  (A NaN key
+//           seen by many rows flags every one of them; this settles them
+//           without float64 dot products over the whole window.)
+//   pass 1  the float64 NaN-propagating maximum score M;
+//   pass 2  w_j = exp(s_j - M) block by block and sum_j w_j v_j in key order,
+//           one thread per output dim.
+// Key j always goes to thread (j - lo) mod 256 and the reductions use fixed
+// trees, so the bits depend only on the row's own inputs.
 #include <cuda_bf16.h>
 
 #include "wa_internal.h"
@@ -68,8 +78,41 @@ __device__ __forceinline__ double block_reduce(double x, bool is_max, double* re
     return r;
 }
 
+// d bf16 values of a row as float64 (16-byte loads; the row is 16-byte aligned).
+__device__ __forceinline__ double dot_f64(const double* qd, const uint16_t* kr, int d) {
+    double s = 0.0;
+    for (int e = 0; e < d; e += 8) {
+        const uint4 u = *reinterpret_cast<const uint4*>(kr + e);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            s = s + qd[e + 2 * i] * static_cast<double>(__uint_as_float(w[i] << 16));
+            s = s + qd[e + 2 * i + 1] * static_cast<double>(__uint_as_float(w[i] & 0xFFFF0000u));
+        }
+    }
+    return s;
+}
+
+// The same dot product in fp32: every product of two bf16 values is exact in fp32 unless it
+// overflows or underflows, so a finite float64 score can only come out non-finite here through
+// overflow, and a float64 NaN or infinity always shows as non-finite.
+__device__ __forceinline__ float dot_f32(const float* qf, const uint16_t* kr, int d) {
+    float s = 0.f;
+    for (int e = 0; e < d; e += 8) {
+        const uint4 u = *reinterpret_cast<const uint4*>(kr + e);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            s = fmaf(qf[e + 2 * i], __uint_as_float(w[i] << 16), s);
+            s = fmaf(qf[e + 2 * i + 1], __uint_as_float(w[i] & 0xFFFF0000u), s);
+        }
+    }
+    return s;
+}
+
 __global__ void __launch_bounds__(kRerunThreads) rerun_f64_kernel(RerunArgs a) {
     __shared__ double qd[256];
+    __shared__ float qf[256];
     __shared__ double wb[kRerunThreads];
     __shared__ double red[kRerunThreads / 32];
     __shared__ int sel_row[64];
@@ -113,7 +156,11 @@ __global__ void __launch_bounds__(kRerunThreads) rerun_f64_kernel(RerunArgs a) {
             vst = a.v_tok;
             orow = out + row * a.o_tok + static_cast<int64_t>(h) * d;
         }
-        if (t < d) qd[t] = bf16_bits_to_f64(qrow[t]);
+        if (t < d) {
+            const float x = __uint_as_float(static_cast<uint32_t>(qrow[t]) << 16);
+            qf[t] = x * a.scale;   // the scale applied to fp32 q: only the class of the score matters here
+            qd[t] = static_cast<double>(x);
+        }
         const int nsel = a.mode == 2 ? a.nsel : 0;
         if (t < nsel) sel_row[t] = a.sel[(static_cast<int64_t>(row) * a.hkv + g) * a.nsel + t];
         __syncthreads();
@@ -124,15 +171,36 @@ __global__ void __launch_bounds__(kRerunThreads) rerun_f64_kernel(RerunArgs a) {
             for (int e = 0; e < nsel; ++e) hit |= sel_row[e] == (j >> 6);
             return hit;
         };
+        auto score = [&](int j) {
+            const uint16_t* kr = kb + static_cast<int64_t>(j % a.ring) * kst;
+            return dot_f64(qd, kr, d) * static_cast<double>(a.scale);
+        };
+
+        // pass 0: a float64 score that is NaN or +inf makes the output NaN
+        bool nan_out = false;
+        for (int base = lo; base <= last && !nan_out; base += kRerunThreads) {
+            const int j = base + t;
+            bool hit = false;
+            if (j <= last && selected(j)) {
+                const float sf = dot_f32(qf, kb + static_cast<int64_t>(j % a.ring) * kst, d);
+                if (!isfinite(sf)) {
+                    const double s = score(j);
+                    hit = isnan(s) || (isinf(s) && s > 0.0);
+                }
+            }
+            nan_out = __syncthreads_or(hit) != 0;
+        }
+        if (nan_out) {
+            if (t < d) orow[t] = 0x7FC0u;
+            __syncthreads();
+            continue;
+        }
 
         // pass 1: the maximum score (NaN if any score is NaN)
         double mloc = -INFINITY;
         for (int j = lo + t; j <= last; j += kRerunThreads) {
             if (!selected(j)) continue;
-            const uint16_t* kr = kb + static_cast<int64_t>(j % a.ring) * kst;
-            double s = 0.0;
-            for (int e = 0; e < d; ++e) s = s + qd[e] * bf16_bits_to_f64(kr[e]);
-            s = s * static_cast<double>(a.scale);
+            const double s = score(j);
             mloc = (isnan(s) || isnan(mloc)) ? (s + mloc) : fmax(mloc, s);
         }
         const double M = block_reduce(mloc, true, red);
@@ -144,11 +212,7 @@ __global__ void __launch_bounds__(kRerunThreads) rerun_f64_kernel(RerunArgs a) {
             double w = 0.0;
             const bool use = j <= last && selected(j);
             if (use) {
-                const uint16_t* kr = kb + static_cast<int64_t>(j % a.ring) * kst;
-                double s = 0.0;
-                for (int e = 0; e < d; ++e) s = s + qd[e] * bf16_bits_to_f64(kr[e]);
-                s = s * static_cast<double>(a.scale);
-                w = exp(s - M);
+                w = exp(score(j) - M);
                 lloc = lloc + w;
             }
             wb[t] = w;
@@ -170,8 +234,15 @@ __global__ void __launch_bounds__(kRerunThreads) rerun_f64_kernel(RerunArgs a) {
 
 }  // namespace
 
+// A few CTAs per SM, never more than the (row, head) pairs that can be flagged: the grid is
+// fixed before the flag count is known (no host read), and CTAs past the count exit at once.
 cudaError_t launch_rerun(const RerunArgs& a, cudaStream_t s) {
-    rerun_f64_kernel<<<64, kRerunThreads, 0, s>>>(a);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidValue;
+    const int64_t units = static_cast<int64_t>(a.rows) * a.hq;
+    const int grid = static_cast<int>(units < 4LL * sms ? units : 4LL * sms);
+    rerun_f64_kernel<<<grid, kRerunThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
