@@ -1,11 +1,13 @@
 // wa_prompt.cu — prompt form (dense rows): instantiations, the tensor-map encoder, launches.
 //
-// The kernels are in wa_prompt_kernel.cuh (head dim 256, and three P parts at 128) and
-// wa_prompt_pair.cuh (head dim 128 with one or two P parts); see there for the designs and sources.
+// The kernels are in wa_prompt_d256.cuh (head dim 256 with one or two P parts),
+// wa_prompt_pair.cuh (head dim 128 with one or two P parts) and wa_prompt_kernel.cuh (three P
+// parts at either head dim); see there for the designs and sources.
 #include <mutex>
 
 #include "wa_prompt_kernel.cuh"
 #include "wa_prompt_pair.cuh"
+#include "wa_prompt_d256.cuh"
 
 namespace wa {
 
@@ -28,8 +30,8 @@ cudaError_t prompt_prepare_device(int) {
     if ((e = set_pair_attr<1>()) != cudaSuccess) return e;
     if ((e = set_pair_attr<2>()) != cudaSuccess) return e;
     if ((e = set_attr<128, 3>()) != cudaSuccess) return e;
-    if ((e = set_attr<256, 1>()) != cudaSuccess) return e;
-    if ((e = set_attr<256, 2>()) != cudaSuccess) return e;
+    if ((e = set_d256_attr<1>()) != cudaSuccess) return e;
+    if ((e = set_d256_attr<2>()) != cudaSuccess) return e;
     return set_attr<256, 3>();
 }
 
@@ -37,7 +39,7 @@ cudaError_t launch_prompt(const PromptArgs& a, cudaStream_t s) {
     if (get_encoder() != cudaSuccess) return cudaErrorNotSupported;
     if (a.d == 256) {
         if (a.p32 == 2) return launch_t<256, 3, false>(a, s);
-        return a.p32 ? launch_t<256, 2, false>(a, s) : launch_t<256, 1, false>(a, s);
+        return a.p32 ? launch_d256<2>(a, s) : launch_d256<1>(a, s);
     }
     if (a.p32 == 2) return launch_t<128, 3, false>(a, s);
     return a.p32 ? launch_pair<2>(a, s) : launch_pair<1>(a, s);

@@ -139,8 +139,10 @@ def test_chunk_split_gives_every_rows_bits(wa):
 
 
 @pytest.mark.parametrize("d,p32", [(256, 0), (256, 1), (256, 2), (128, 2)])
-def test_every_block_selected_gives_the_dense_bits(wa, d, p32):
-    """Both forms then run the same 64-key tiles in key order for every row."""
+def test_every_block_selected_gives_the_dense_result(wa, d, p32):
+    """With three P parts both forms run the same 64-key tiles in key order for every row, so the
+    bits agree; with one or two parts the dense form at head dim 256 runs 128-key tiles (another
+    fp32 summation order), so both are held to the oracle instead."""
     n, p0, hq, hkv, win, ring = 200, 1500, 8, 2, 1024, 1536
     c = _case(n, p0, hq, hkv, d, win, ring, seed=13)
     nb = (p0 + n - 1) // 64 + 1
@@ -149,7 +151,13 @@ def test_every_block_selected_gives_the_dense_bits(wa, d, p32):
     assert nb - lo_b <= 64
     sparse = wa.prompt_sparse(c["q"], c["k"], c["v"], p0, sel, None, win, 1.0, p32=p32)
     dense = wa.prompt(c["q"], c["k"], c["v"], p0, None, win, 1.0, p32=p32)
-    assert torch.equal(sparse.view(torch.int16), dense.view(torch.int16))
+    if p32 == 2:
+        assert torch.equal(sparse.view(torch.int16), dense.view(torch.int16))
+    else:
+        ref = oracle.prompt(bits(c["q"]), bits(c["k"]), bits(c["v"]), p0, win, ring, 1.0)
+        tol = check.TOL_P32 if p32 else check.TOL_BF16_P
+        assert_parity(sparse, ref, tol, "sparse, every block")
+        assert_parity(dense, ref, tol, "dense")
 
 
 def test_served_size_sampled(wa):
