@@ -178,10 +178,11 @@ decode_part_kernel(const __grid_constant__ RingMaps maps,
             }
             issued = t + 1;
         }
-        if (!ok && lane == 0) {
-            // a consumer stopped: let the copies already issued land before the CTA can exit
+        // Let the copies already issued land before this warp exits, whichever role stopped early
+        // (when every load was consumed these barriers have completed and the waits return at once).
+        if (lane == 0)
             for (int t = max(0, issued - C::STAGES); t < issued; ++t) mbar_wait(bar_full + 8 * t, 0, status);
-        }
+        (void)ok;
         return;
     }
 

@@ -229,7 +229,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
                 }
             }
         }
-        if (!ok && lane == 0) {   // a wait ran out: let the copies in flight land before the block exits
+        // let the copies in flight land before the block exits, whichever role stopped early (after a
+        // normal run every one was consumed, and the waits return at once)
+        if (lane == 0) {
             for (int t = max(0, issued[0] - C::NSK); t < issued[0]; ++t)
                 mbar_wait(BAR(C::B_KFULL + t % C::NSK), (t / C::NSK) & 1, p.status);
             for (int t = max(0, issued[1] - C::NSV); t < issued[1]; ++t)

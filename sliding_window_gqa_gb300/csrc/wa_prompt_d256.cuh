@@ -257,9 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_d256_kernel(const __grid_c
             __syncwarp();
             issued = u + 1;
         }
-        if (!ok && lane == 0) {
-            // let every copy already issued land before the CTA can exit: the last NSLOT loads
-            // hold one slot each
+        if (lane == 0) {
+            // let every copy already issued land before the CTA can exit, whichever role stopped
+            // early (after a normal run every one was consumed, and the waits return at once): the
+            // last NSLOT loads hold one slot each
             mbar_wait(BAR(WB_Q), 0, p.status);
             for (int u = max(0, issued - C::NSLOT); u < issued; ++u)
                 mbar_wait(BAR(WB_FULL + u % C::NSLOT), (u / C::NSLOT) & 1, p.status);

@@ -443,8 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_kernel(const __grid_consta
             }
             issued = idx + 1;
         }
-        if (!ok && lane == 0) {
-            // let every TMA copy already issued land before the CTA can exit
+        if (lane == 0) {
+            // let every TMA copy already issued land before the CTA can exit, whichever role stopped
+            // early (after a normal run every one was consumed, and the waits return at once)
             mbar_wait(BAR(B_Q), 0, p.status);
             for (int idx = max(0, issued - 2); idx < issued; ++idx) {
                 mbar_wait(BAR(B_KFULL + (idx & 1)), (idx >> 1) & 1, p.status);
