@@ -79,8 +79,12 @@ SPEC = {
 
 # ncu DRAM bytes per launch of the dominant kernels, valid only while the kernel source is unchanged.
 TRAFFIC = {
-    "prompt_dense": {"bytes_per_launch": 2059 * 10**6, "source_sha": "f344a5021ad67644",
-                     "note": "ncu at N=8192 (352.5 MB read + 93.5 MB write), scaled by N to 37,810"},
+    "prompt_dense": {"bytes_per_launch": 2057 * 10**6, "source_sha": "68921256d3482bf8",
+                     "note": "ncu at N=8192 (352.5 MB read + 93.1 MB write), scaled by N to 37,810"},
+    "prompt_dense_p32": {"bytes_per_launch": 2058 * 10**6, "source_sha": "68921256d3482bf8",
+                         "note": "ncu at N=8192 (352.6 MB read + 93.3 MB write), scaled by N to 37,810"},
+    "prompt_causal": {"bytes_per_launch": 211 * 10**6, "source_sha": "9e6653458f422865",
+                      "note": "ncu of the full launch (186.1 MB read + 25.4 MB write)"},
     "decode_gqa8": {"bytes_per_launch": 853 * 10**6, "source_sha": "2033d7ed7d9eaec4",
                     "note": "the part's three launches together, like its achieved figure: ncu at 256 rows, one cache "
                             "(1.134 GB read + 8.0 MB write for 1.072 GB algorithmic), scaled by algorithmic bytes "
@@ -566,7 +570,7 @@ PART_CLASSES = {"decode_sliding": DecodeSliding, "decode_linear": DecodeLinear,
                 "prompt_sparse": PromptSparse}
 
 KERNEL_OF = {"decode_sliding": "decode partial (wa_decode.cu)", "decode_linear": "decode partial (wa_decode.cu)",
-             "prompt_causal": "prompt tensor-core tile (wa_prompt_kernel.cuh)",
+             "prompt_causal": "prompt tensor-core tile, 128-key tiles (wa_prompt_d256.cuh)",
              "prompt_dense": "prompt tensor-core tiles, two query tiles a CTA (wa_prompt_pair.cuh)",
              "prompt_dense_p32": "prompt tensor-core tiles, two query tiles a CTA, two P parts (wa_prompt_pair.cuh)",
              "decode_gqa8": "tensor-core decode partial (wa_decode_tc.cu)",
@@ -574,7 +578,7 @@ KERNEL_OF = {"decode_sliding": "decode partial (wa_decode.cu)", "decode_linear":
              "prep_dense": "q/k preparation (wa_prep.cu)",
              "prompt_sparse": "block-sparse prompt tile (wa_prompt_sparse.cu)"}
 SOURCE_OF = {"decode_sliding": "wa_decode.cu", "decode_linear": "wa_decode.cu",
-             "prompt_causal": "wa_prompt_kernel.cuh", "prompt_dense": "wa_prompt_pair.cuh",
+             "prompt_causal": "wa_prompt_d256.cuh", "prompt_dense": "wa_prompt_pair.cuh",
              "prompt_dense_p32": "wa_prompt_pair.cuh",
              "decode_gqa8": "wa_decode_tc.cu", "decode_gqa16_linear": "wa_decode_tc.cu",
              "prep_dense": "wa_prep.cu", "prompt_sparse": "wa_prompt_kernel.cuh"}
