@@ -65,12 +65,17 @@ struct WideCfg {
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// Barrier indices.  FULL/FREE per ring slot; [b] = per key-tile parity (tile & 1); VREADY per
-// V half and tile parity.  A parity wait for phase k is only sound while phase k + 1 cannot have
-// completed; every barrier here that can run a tile ahead of its waiter is kept per parity.
+// Barrier indices.  FREE per ring slot (the producer takes every use of a slot in order); [b] = per
+// key-tile parity (tile & 1); KFULL, VFULL and VREADY per operand half and tile parity.  A parity
+// wait for phase k is only sound while the barrier has completed phase k - 1 and cannot have
+// completed phase k + 1.  A slot holds K and V halves in turn, so a per-slot "loaded" barrier would
+// let the V sanitizer (which waits for V halves only) meet a slot whose previous, K, load had not
+// landed yet and take that phase for its own; loads therefore signal per operand half and tile
+// parity, whose phases each waiter takes in order.
 enum : int {
-    WB_Q = 0, WB_FULL = 1, WB_FREE = 6, WB_SFULL = 11, WB_PVDONE = 13, WB_VREADY = 15,   // VREADY [half][b]
-    WB_XCHG = 19, WB_PHALF = 21, WB_PFULL = 23, WB_EPI_L = 25, WB_EPI_B = 26, WB_DRAIN = 27
+    WB_Q = 0, WB_KFULL = 1, WB_VFULL = 5, WB_FREE = 9, WB_SFULL = 14, WB_PVDONE = 16,   // K/VFULL [half][b]
+    WB_VREADY = 18,  // [half][b]
+    WB_XCHG = 22, WB_PHALF = 24, WB_PFULL = 26, WB_EPI_L = 28, WB_EPI_B = 29, WB_DRAIN = 30
 };
 
 // The ring's load sequence is K0, then for each tile j: K(j + 1) if it exists, then V(j).
@@ -127,9 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_d256_kernel(const __grid_c
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(WB_Q), 1);
-        for (int s = 0; s < C::NSLOT; ++s) {
-            mbar_init(BAR(WB_FULL + s), 1);
-            mbar_init(BAR(WB_FREE + s), 1);
+        for (int s = 0; s < C::NSLOT; ++s) mbar_init(BAR(WB_FREE + s), 1);
+        for (int x = 0; x < 4; ++x) {
+            mbar_init(BAR(WB_KFULL + x), 1);      // [half][b]: TMA bytes, or one arrival after a warp copy
+            mbar_init(BAR(WB_VFULL + x), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(BAR(WB_SFULL + b), 1);      // MMA commits
@@ -209,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_d256_kernel(const __grid_c
         const uint64_t pol_kv = policy_evict_last();
         bool ok = true;
         int issued = 0;
+        int lastbar[C::NSLOT], lastph[C::NSLOT];   // the barrier and phase of the load in each slot
         for (int u = 0; u < nhalf && ok; ++u) {
             const int o = u >> 1, half = u & 1;
             // operand o of the sequence K0, K1, V0, K2, V1, ...: K(t) or V(t)
@@ -229,7 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_d256_kernel(const __grid_c
                 ok = false;
                 break;
             }
-            const uint32_t full = BAR(WB_FULL + s);
+            // loaded: signalled per operand half and tile parity
+            const int fb = (is_v ? WB_VFULL : WB_KFULL) + 2 * half + (t & 1);
+            lastbar[s] = fb;
+            lastph[s] = (t >> 1) & 1;
+            const uint32_t full = BAR(fb);
             const uint32_t dst = SLOT(s);
             const int key0 = (j0 + t) * T + (is_v ? half * 64 : 0);
             const int nkeys = is_v ? 64 : T;
@@ -263,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_d256_kernel(const __grid_c
             // last NSLOT loads hold one slot each
             mbar_wait(BAR(WB_Q), 0, p.status);
             for (int u = max(0, issued - C::NSLOT); u < issued; ++u)
-                mbar_wait(BAR(WB_FULL + u % C::NSLOT), (u / C::NSLOT) & 1, p.status);
+                mbar_wait(BAR(lastbar[u % C::NSLOT]), lastph[u % C::NSLOT], p.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (one thread)
@@ -278,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_d256_kernel(const __grid_c
 #pragma unroll
                 for (int kh = 0; kh < 2; ++kh) {
                     const int u = 2 * op_of_k(t) + kh, s = u % C::NSLOT;
-                    if (!mbar_wait(BAR(WB_FULL + s), (u / C::NSLOT) & 1, p.status)) return false;
+                    if (!mbar_wait(BAR(WB_KFULL + 2 * kh + (t & 1)), (t >> 1) & 1, p.status)) return false;
                     tc_fence_after();
                     const uint64_t bk = sdesc_sw128(SLOT(s), 16, 1024);
 #pragma unroll
@@ -330,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_d256_kernel(const __grid_c
             bool ok = true;
             for (int hh = 0; hh < 2; ++hh) {
                 const int u = 2 * op_of_v(t, ntiles) + hh, s = u % C::NSLOT;
-                if (!warp_wait(BAR(WB_FULL + s), (u / C::NSLOT) & 1, p.status)) {
+                if (!warp_wait(BAR(WB_VFULL + 2 * hh + (t & 1)), (t >> 1) & 1, p.status)) {
                     ok = false;
                     break;
                 }
