@@ -508,6 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_d256_kernel(const __grid_c
         }
         if (ok) {
             const float l = xl[r] + xl[kBM + r];
+            // o = O / l as O times the correctly rounded 1 / l: within one fp32 ulp of the quotient,
+            // far inside the bf16 rounding that follows, for one division a row instead of d / 2
+            const float inv_l = __fdiv_rn(1.f, l);
             tc_fence_after();
             bool bad = false;
             uint16_t* orow = p.out + static_cast<int64_t>(i) * p.o_tok + static_cast<int64_t>(h) * D + wg * 128;
@@ -518,8 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_d256_kernel(const __grid_c
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float a = __fdiv_rn(__uint_as_float(o[2 * e]), l);
-                    const float bb = __fdiv_rn(__uint_as_float(o[2 * e + 1]), l);
+                    const float a = __uint_as_float(o[2 * e]) * inv_l;
+                    const float bb = __uint_as_float(o[2 * e + 1]) * inv_l;
                     bad |= !(isfinite(a) && isfinite(bb));
                     pk[e] = pack_bf16(a, bb);
                 }
