@@ -419,9 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_pair_kernel(const __grid_c
         if (ok) {
             tc_fence_after();
             bool bad = false;
-            // o = O / l as O times the correctly rounded 1 / l: within one fp32 ulp of the quotient,
-            // far inside the bf16 rounding that follows, for one division a row instead of d
-            const float inv_l = __fdiv_rn(1.f, l_run);
             uint16_t* orow = p.out + static_cast<int64_t>(i) * p.o_tok + static_cast<int64_t>(h) * D;
 #pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
@@ -430,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_pair_kernel(const __grid_c
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float a = __uint_as_float(o[2 * e]) * inv_l;
-                    const float b = __uint_as_float(o[2 * e + 1]) * inv_l;
+                    const float a = __fdiv_rn(__uint_as_float(o[2 * e]), l_run);
+                    const float b = __fdiv_rn(__uint_as_float(o[2 * e + 1]), l_run);
                     bad |= !(isfinite(a) && isfinite(b));
                     pk[e] = pack_bf16(a, b);
                 }
