@@ -301,6 +301,34 @@ class Part:
     def collect(self):
         self.kernel_ms.append(self.k_start.elapsed_time(self.k_end))
 
+    _copy_streams = None
+
+    def h2d(self, dst, src):
+        """dst <- src (pinned host) on the current stream; a large tensor goes as four chunks along
+        its first dim on helper streams, which the current stream then waits for, so its bytes
+        spread over the copy engines."""
+        torch = self.torch
+        cur = torch.cuda.current_stream()
+        if dst.dim() == 0 or dst.shape[0] < 4 or dst.numel() * dst.element_size() < (256 << 20):
+            dst.copy_(src, non_blocking=True)
+            return
+        if self._copy_streams is None:
+            self._copy_streams = [torch.cuda.Stream(device=dst.device) for _ in range(4)]
+        start = torch.cuda.Event()
+        start.record(cur)
+        n = dst.shape[0]
+        per = (n + 3) // 4
+        for k, cs in enumerate(self._copy_streams):
+            a, b = k * per, min(n, (k + 1) * per)
+            if a >= b:
+                continue
+            cs.wait_event(start)
+            with torch.cuda.stream(cs):
+                dst[a:b].copy_(src[a:b], non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(cs)
+            cur.wait_event(done)
+
 
 def _events(torch, stream, n=2):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -362,7 +390,7 @@ class DecodeSliding(Part):
             with torch.cuda.stream(st):
                 if host is not None:
                     for key in ("q", "k", "v", "pos"):
-                        c[key].copy_(host[i][key], non_blocking=True)
+                        self.h2d(c[key], host[i][key])
                 wa.decode(c["q"], c["k"], c["v"], c["pos"], s["win"], 1.0, out=self.outs[i], ws=self.ws[i], stream=st)
                 if host is not None:
                     host[i]["out"].copy_(self.outs[i], non_blocking=True)
@@ -412,7 +440,7 @@ class DecodeLinear(Part):
 
     def copy_in(self, host):
         for key in ("q", "k", "v", "pos"):
-            self.c[key].copy_(host[key], non_blocking=True)
+            self.h2d(self.c[key], host[key])
 
     def copy_out(self, host):
         host["out"].copy_(self.out, non_blocking=True)
@@ -444,7 +472,7 @@ class PromptCausal(Part):
 
     def copy_in(self, host):
         for key in ("q", "k", "v"):
-            self.c[key].copy_(host[key], non_blocking=True)
+            self.h2d(self.c[key], host[key])
 
     def copy_out(self, host):
         host["out"].copy_(self.out, non_blocking=True)
@@ -475,7 +503,7 @@ class PromptDense(Part):
                        stream=stream)
 
     def copy_in(self, host):
-        self.c["qkv"].copy_(host["qkv"], non_blocking=True)
+        self.h2d(self.c["qkv"], host["qkv"])
         self.hi.copy_(host["hi"], non_blocking=True)
 
     def copy_out(self, host):
