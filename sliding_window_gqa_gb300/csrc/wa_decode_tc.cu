@@ -7,9 +7,17 @@
 // large enough (the pages allow up to 16) that scoring on CUDA cores, not HBM,
 // bounds the CUDA-core kernel.
 //
-// GB300 design.  A persistent grid, one CTA per SM; CTA b takes the units
-// (row, key head, chunk) b, b + grid, b + 2 grid, ... and streams their K and V
-// through shared-memory rings without a break between units.  160 threads:
+// GB300 design.  A persistent grid, one CTA per SM, that streams the K and V of
+// its units (row, key head, chunk) through shared-memory rings without a break
+// between units.  Units come from a counter in the workspace header, long ones
+// first: each CTA's producer warp sorts the rows by chunk count (a counting sort
+// in shared memory) and walks "levels" from the last: level e holds, for every
+// row with more than e chunks, the chunk e places from its end, where the order
+// from the end is last chunk, first chunk, then the middle ones.  Whole chunks go
+// first, the ragged first and last chunks last, and no empty chunk is taken
+// (calls too large for the sort take units in a plain stride).  The producer
+// hands each unit, fully described, to the other warps through a ring of unit
+// slots, so no other role reads the positions.  160 threads:
 //   warp 0  softmax, one lane per query head of the group (tensor-memory lane
 //           h = head h; M = 128 with the lanes past the group unused): an
 //           online softmax over the chunk's 64-key sub-tiles at absolute
@@ -18,9 +26,9 @@
 //   warp 1  allocates tensor memory; lane 0 issues tcgen05.mma:
 //           S = Q K^T (A = Q from tensor memory, B = K, 128-byte swizzle) and
 //           O += P V (A = P from tensor memory, B = V read MN-major).
-//   warp 2  TMA producer: K and V sub-tiles through rings of stages; a
-//           sub-tile that wraps around the ring is copied by the warp with
-//           the same swizzle.
+//   warp 2  takes units and publishes them; TMA producer: K and V sub-tiles
+//           through rings of stages; a sub-tile that wraps around the ring is
+//           copied by the warp with the same swizzle.
 //   warp 3  zeroes V rows outside the row's window, so a stale ring slot
 //           never meets a zero probability as 0 * inf.
 //   warp 4  stages each unit's G query heads into tensor memory (negated for
@@ -43,6 +51,9 @@ namespace {
 
 constexpr int kSub = 64;          // keys per sub-tile
 constexpr int kTcThreads = 160;
+constexpr int kUnitSlots = 8;     // units published ahead of the slowest role
+constexpr int kPlanRows = 4096;      // the sorted schedule serves calls up to this many rows ...
+constexpr int kPlanChunks = 1024;    // ... and chunks a row; larger calls take units in a plain stride
 constexpr float kLazyTc = 8.0f;   // log2 units the running max may trail before O is rescaled
 
 struct TcParams {
@@ -53,6 +64,7 @@ struct TcParams {
     const int32_t* pos;
     float* part;
     int* status;
+    int* next_unit;               // zeroed with the workspace header every call
     int rows, hq, hkv, gsize, win, ring, cmax;
     float c;                      // |scale| * log2(e)
     uint32_t qsign;               // 0x80008000 when scale < 0
@@ -81,9 +93,16 @@ struct TcCfg {
     static constexpr int B_ODONE = B_PVDONE + 1;   // last P V of a unit done
     static constexpr int B_OFREE = B_ODONE + 1;    // O of a unit copied out
     static constexpr int B_DRAIN = B_OFREE + 1;
-    static constexpr int NBAR = B_DRAIN + 1;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_MISC + 16;
+    static constexpr int B_UFULL = B_DRAIN + 1;    // [NU] a unit published in the slot
+    static constexpr int B_UFREE = B_UFULL + kUnitSlots;   // [NU] the slot read by the 4 other roles
+    static constexpr int NBAR = B_UFREE + kUnitSlots;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;    // [0] tensor-memory base
+    static constexpr int OFF_RING = OFF_MISC + 16;         // kUnitSlots units (8 ints each)
+    static constexpr int OFF_PERM = OFF_RING + 32 * kUnitSlots;  // kPlanRows: row | chunks << 16, by chunks, descending
+    static constexpr int OFF_CUR = OFF_PERM + 4 * kPlanRows;     // kPlanChunks + 1: histogram, then sort cursors
+    static constexpr int OFF_ACC = OFF_CUR + 4 * (kPlanChunks + 1);     // kPlanChunks: rows in level 0, 1, ...
+    static constexpr int OFF_START = OFF_ACC + 4 * kPlanChunks;          // kPlanChunks + 1: first unit of each level
+    static constexpr int SMEM = OFF_START + 4 * (kPlanChunks + 1);
     // tensor memory: O (D columns), S (64), P hi and lo (2 x 32), Q (D / 2)
     static constexpr int O_COL = 0;
     static constexpr int S_COL = D;
@@ -146,6 +165,24 @@ __device__ __forceinline__ bool unit_at(const TcParams& p, int u, Unit& x, bool 
     return true;
 }
 
+// Chunks holding any of row r's keys (at least 1), with unit_at's clamping.
+__device__ __forceinline__ int row_chunks(const TcParams& p, int r) {
+    int pp = p.pos[r];
+    if (pp < 0 || (p.win == 0 && pp >= p.ring)) pp = pp < 0 ? 0 : p.ring - 1;
+    const int lo = p.win > 0 ? max(0, pp - p.win + 1) : 0;
+    return min(p.cmax, pp / kChunk - lo / kChunk + 1);
+}
+
+// Inclusive sum over the warp's lanes.
+__device__ __forceinline__ int warp_scan_incl(int v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_constant__ TcParams p) {
     using C = TcCfg<D>;
@@ -162,7 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::NBAR; ++i) mbar_init(BAR(i), 1);
+        for (int i = 0; i < C::NBAR; ++i) mbar_init(BAR(i), (i >= C::B_UFREE && i < C::B_UFREE + kUnitSlots) ? 4 : 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -173,21 +210,131 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = misc[0];
+    volatile int* uring = reinterpret_cast<volatile int*>(smem + C::OFF_RING);   // 8 ints a slot
+
+    // Every role but the producer: the U-th published unit (x.nt = 0 after the last).  The MMA
+    // role runs on one thread (whole = false), the others as a warp; each role arrives once.
+    auto take_unit = [&](int U, Unit& x, bool whole) -> bool {
+        const int sl = U % kUnitSlots;
+        const uint32_t ph = static_cast<uint32_t>(U / kUnitSlots) & 1u;
+        if (!(whole ? warp_wait(BAR(C::B_UFULL + sl), ph, p.status) : mbar_wait(BAR(C::B_UFULL + sl), ph, p.status)))
+            return false;
+        volatile int* e = uring + 8 * sl;
+        x.r = e[0]; x.g = e[1]; x.ci = e[2]; x.cbase = e[3];
+        x.kb = e[4]; x.ke = e[5]; x.t0 = e[6]; x.nt = e[7];
+        if (whole) __syncwarp();
+        if (!whole || lane == 0) mbar_arrive(BAR(C::B_UFREE + sl));
+        return true;
+    };
 
     if (warp == 2) {
-        // ------------------------------------------------ TMA producer: K then V of each sub-tile
+        // ------------------------------------------------ unit schedule; TMA producer: K then V of each sub-tile
         const uint64_t pol = policy_evict_first();
         if (lane == 0) {
             prefetch_tensormap(&p.tk);
             prefetch_tensormap(&p.tv);
         }
+        uint32_t* perm = reinterpret_cast<uint32_t*>(smem + C::OFF_PERM);
+        int* cur = reinterpret_cast<int*>(smem + C::OFF_CUR);
+        int* acc = reinterpret_cast<int*>(smem + C::OFF_ACC);
+        int* start = reinterpret_cast<int*>(smem + C::OFF_START);
+        const int cm = p.cmax;
+        const bool planned = p.rows <= kPlanRows && cm <= kPlanChunks;
+        int total = 0;
+        if (planned) {
+            // rows sorted by chunk count, descending (counting sort)
+            for (int c = lane; c <= cm; c += 32) cur[c] = 0;
+            __syncwarp();
+            for (int r = lane; r < p.rows; r += 32) atomicAdd(&cur[row_chunks(p, r)], 1);
+            __syncwarp();
+            // level l takes the chunk e = cm - 1 - l places from each row's end; acc[l] = rows with more than e chunks
+            int carry = 0;
+            for (int b = 0; b < cm; b += 32) {
+                const int i = b + lane;
+                const int v = warp_scan_incl(i < cm ? cur[cm - i] : 0, lane) + carry;
+                if (i < cm) acc[i] = v;
+                carry = __shfl_sync(0xFFFFFFFFu, v, 31);
+            }
+            __syncwarp();
+            // start[l] = units before level l (hkv units per row of a level)
+            carry = 0;
+            for (int b = 0; b < cm; b += 32) {
+                const int i = b + lane;
+                const int a = i < cm ? acc[i] : 0;
+                const int v = warp_scan_incl(a, lane);
+                if (i < cm) start[i] = p.hkv * (carry + v - a);
+                carry += __shfl_sync(0xFFFFFFFFu, v, 31);
+            }
+            if (lane == 0) start[cm] = p.hkv * carry;
+            // rows with n chunks go after every row with more
+            for (int c = lane; c <= cm; c += 32) cur[c] = c >= cm ? 0 : acc[cm - 1 - c];
+            __syncwarp();
+            for (int r = lane; r < p.rows; r += 32) {
+                const int n = row_chunks(p, r);
+                perm[atomicAdd(&cur[n], 1)] = static_cast<uint32_t>(r) | (static_cast<uint32_t>(n) << 16);
+            }
+            __syncwarp();
+            total = start[cm];
+        }
+        // unit k of the schedule: the row's chunks from its end are last, first, then the middle ones
+        auto unit_of = [&](int k) -> int {
+            int lo = 0, hi = cm - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (start[mid] <= k) lo = mid; else hi = mid - 1;
+            }
+            const int e = cm - 1 - lo, j = k - start[lo];
+            const uint32_t ent = perm[j / p.hkv];
+            const int r = static_cast<int>(ent & 0xFFFFu), n = static_cast<int>(ent >> 16), g = j % p.hkv;
+            const int rank = n - 1 - e;
+            const int ci = rank == n - 1 ? n - 1 : (rank == n - 2 ? 0 : rank + 1);
+            return (r * p.hkv + g) * cm + ci;
+        };
+        // A CTA's first unit is its index; each later one comes from the counter, asked one unit
+        // ahead so its answer is back before it is needed.  Without a schedule: a plain stride.
+        int k_cur = blockIdx.x, k_ans = 0, su = blockIdx.x;
+        bool asked = false;
+        auto next_unit = [&]() -> int {
+            if (planned) {
+                if (asked) k_cur = __shfl_sync(0xFFFFFFFFu, k_ans, 0) + static_cast<int>(gridDim.x);
+                if (k_cur >= total) return -1;
+                if (lane == 0) k_ans = atomicAdd(p.next_unit, 1);
+                asked = true;
+                return unit_of(k_cur);
+            }
+            const int u = su < units ? su : -1;
+            su += gridDim.x;
+            return u;
+        };
+        int Upub = 0;
+        auto publish = [&](const Unit& x) -> bool {
+            const int sl = Upub % kUnitSlots;
+            if (Upub >= kUnitSlots &&
+                !warp_wait(BAR(C::B_UFREE + sl), static_cast<uint32_t>(Upub / kUnitSlots - 1) & 1u, p.status))
+                return false;
+            if (lane == 0) {
+                volatile int* e = uring + 8 * sl;
+                e[0] = x.r; e[1] = x.g; e[2] = x.ci; e[3] = x.cbase;
+                e[4] = x.kb; e[5] = x.ke; e[6] = x.t0; e[7] = x.nt;
+                mbar_arrive(BAR(C::B_UFULL + sl));
+            }
+            __syncwarp();
+            ++Upub;
+            return true;
+        };
         const size_t row_elems = static_cast<size_t>(p.ring) * p.hkv * D;
         bool ok = true;
         int issued[2] = {0, 0};
         int T = 0;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            Unit x;
-            if (!unit_at(p, u, x, false)) continue;
+        while (ok) {
+            const int u = next_unit();
+            Unit x{};
+            if (u >= 0 && !unit_at(p, u, x, lane == 0)) continue;   // an empty chunk (stride only)
+            if (!publish(x)) {   // x.nt = 0: the end
+                ok = false;
+                break;
+            }
+            if (u < 0) break;
             for (int idx = 0; idx < x.nt && ok; ++idx, ++T) {
                 const int key0 = x.cbase + (x.t0 + idx) * kSub;
                 const int slot0 = key0 % p.ring;
@@ -268,9 +415,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
                 if (pv_last) mma_commit(BAR(C::B_ODONE));
                 return true;
             };
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            while (ok) {
                 Unit x;
-                if (!unit_at(p, u, x, false)) continue;
+                if (!(ok = take_unit(U, x, false)) || x.nt <= 0) break;
                 ok = mbar_wait(BAR(C::B_QT), U & 1, p.status);
                 for (int idx = 0; idx < x.nt && ok; ++idx, ++T) {
                     const int s = T % C::NSK, use = T / C::NSK;
@@ -305,9 +452,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         // ------------------------------------------------ V rows outside [kb, ke] -> 0
         int T = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        for (int U = 0; ok; ++U) {
             Unit x;
-            if (!unit_at(p, u, x, false)) continue;
+            if (!(ok = take_unit(U, x, true)) || x.nt <= 0) break;
             for (int idx = 0; idx < x.nt; ++idx, ++T) {
                 const int s = T % C::NSV, use = T / C::NSV;
                 if (!warp_wait(BAR(C::B_VFULL + s), use & 1, p.status)) {
@@ -338,29 +485,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         bool ok = true;
         int U = 0;
         float* prev_rec = nullptr;
+        // O of a finished unit into its record: up to 128 columns loaded per wait, and O is handed
+        // back as soon as the last load has landed, before the last stores
         auto copy_out = [&](float* rec, int Uo) -> bool {
             if (!warp_wait(BAR(C::B_ODONE), Uo & 1, p.status)) return false;
             tc_fence_after();
+            constexpr int NB = D >= 128 ? 4 : D / 32;     // 32-column loads per batch
 #pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                tmem_ld32_wait(tbase + C::O_COL + cc * 32, o);
-                if (live) {
-                    float4* dst = reinterpret_cast<float4*>(rec + 4 + cc * 32);
+            for (int cb = 0; cb < D / 32; cb += NB) {
+                uint32_t o[NB][32];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                                             __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                for (int b = 0; b < NB; ++b) tmem_ld32(tbase + C::O_COL + (cb + b) * 32, o[b]);
+                tmem_wait_ld();
+                if (cb + NB >= D / 32) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(C::B_OFREE));
+                }
+                if (live) {
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        float4* dst = reinterpret_cast<float4*>(rec + 4 + (cb + b) * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(o[b][4 * e]), __uint_as_float(o[b][4 * e + 1]),
+                                                 __uint_as_float(o[b][4 * e + 2]), __uint_as_float(o[b][4 * e + 3]));
+                    }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(C::B_OFREE));
             return true;
         };
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        while (ok) {
             Unit x;
-            if (!unit_at(p, u, x, lane == 0)) continue;
+            if (!(ok = take_unit(U, x, true)) || x.nt <= 0) break;
             const size_t head = static_cast<size_t>(x.r) * p.hq + static_cast<size_t>(x.g) * p.gsize + h;
             const uint4* qrow = reinterpret_cast<const uint4*>(p.q + head * D);
             uint4 qv[D / 8];
@@ -399,9 +556,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         const float cl = p.c;
         bool ok = true;
         int T = 0;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        for (int U = 0; ok; ++U) {
             Unit x;
-            if (!unit_at(p, u, x, false)) continue;
+            if (!(ok = take_unit(U, x, true)) || x.nt <= 0) break;
             float m_run = -INFINITY, l_run = 0.f;
             for (int idx = 0; idx < x.nt; ++idx, ++T) {
                 if (!warp_wait(BAR(C::B_SFULL), T & 1, p.status)) {
@@ -416,21 +573,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
                 if (lane == 0) mbar_arrive(BAR(C::B_SFREE));
                 const int key0 = x.cbase + (x.t0 + idx) * kSub;
                 const int vlo = x.kb - key0, vhi = x.ke - key0;   // visible columns [vlo, vhi]
-                float mx = -INFINITY;
+                // eight independent max and sum chains (a chain of 64 would pace the warp)
+                float mx8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
 #pragma unroll
                 for (int k = 0; k < kSub; ++k)
-                    mx = fmaxf(mx, (k >= vlo && k <= vhi) ? __uint_as_float(raw[k]) : -INFINITY);
+                    mx8[k & 7] = fmaxf(mx8[k & 7], (k >= vlo && k <= vhi) ? __uint_as_float(raw[k]) : -INFINITY);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float mt = mx * cl;
                 const float m_new = (mt > m_run + kLazyTc) ? mt : m_run;
                 const float alpha = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
                 const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
                 float pv[kSub];
-                float ls = 0.f;
+                float ls8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ls8[e] = 0.f;
 #pragma unroll
                 for (int k = 0; k < kSub; ++k) {
                     pv[k] = (k >= vlo && k <= vhi) ? ex2(fmaf(__uint_as_float(raw[k]), cl, -m_sub)) : 0.f;
-                    ls += pv[k];                                 // key order within the sub-tile
+                    ls8[k & 7] += pv[k];                         // keys k = e mod 8 in key order
                 }
+                const float ls = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
                 l_run = (alpha == 1.f) ? (l_run + ls) : fmaf(l_run, alpha, ls);
                 m_run = m_new;
                 // P V of the previous sub-tile must be done before P is overwritten (and O rescaled)
@@ -517,6 +682,7 @@ cudaError_t launch_tc_d(const DecodeArgs& a, cudaStream_t s) {
     tp.pos = a.pos;
     tp.part = a.part;
     tp.status = &a.hdr->status;
+    tp.next_unit = &a.hdr->next_unit;
     tp.rows = a.rows; tp.hq = a.hq; tp.hkv = a.hkv; tp.gsize = a.hq / a.hkv; tp.win = a.win; tp.ring = a.ring;
     tp.cmax = a.cmax;
     tp.qsign = a.scale < 0.f ? 0x80008000u : 0u;

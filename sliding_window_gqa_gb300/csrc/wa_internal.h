@@ -16,7 +16,8 @@ constexpr int kHeaderBytes = 256;
 struct WsHeader {
     int status;   // WA_STATUS_* bits
     int nflag;    // (row, head) pairs queued for the float64 re-run
-    int pad[62];
+    int next_unit;   // tensor-core decode: units taken so far past the first one of each CTA
+    int pad[61];
 };
 
 inline int decode_chunks_max(int win, int ring) {

@@ -59,6 +59,10 @@ CASES = [
     ("gqa8_d128_ring333", 2, 8, 1, 128, 300, 333, [299, 1234]),
     ("gqa5_d256", 3, 10, 2, 256, 1024, 1536, [1536, 77, 30000]),
     ("gqa16_d128_many_units", 40, 32, 2, 128, 1024, 1100, list(range(3, 40000, 997))[:40]),
+    # linear caches of 16 chunks or more: units taken from the shared counter, longest first
+    ("gqa8_linear_d128_20_chunks", 5, 16, 2, 128, 0, 5000, [0, 255, 256, 4999, 3000]),
+    ("gqa4_linear_d256_17_chunks", 24, 16, 4, 256, 0, 4100, [0, 1, 255, 256, 257, 511, 512, 4095, 4096, 4099]
+     + list(range(37, 4100, 293))[:14]),
 ]
 
 
@@ -149,6 +153,41 @@ def test_nonfinite_classes_match_float64(wa, plant, hq):
     out = wa.decode(dev["q"], dev["k"], dev["v"], pos, 600, 1.0)
     r = assert_parity(out, ref, TOL, plant)
     assert r["n_nonfinite_ref"] > 0
+
+
+@pytest.mark.parametrize("hkv", [8, 2])
+def test_batch_composition_does_not_change_bits_linear_many_chunks(wa, hkv):
+    pos = [4999, 0, 1300, 256, 4095, 2047]
+    c = _case(6, 16, hkv, 128, 0, 5000, pos, seed=14)
+    full = wa.decode(c["q"], c["k"], c["v"], c["pos"], 0, 1.0)
+    for order in ([5, 4, 3, 2, 1, 0], [0], [1, 4], [2, 3, 5]):
+        sel = torch.tensor(order, device="cuda")
+        part = wa.decode(c["q"][sel].contiguous(), c["k"][sel].contiguous(), c["v"][sel].contiguous(),
+                         c["pos"][sel].contiguous(), 0, 1.0)
+        assert torch.equal(part.view(torch.int16), full[sel].view(torch.int16)), order
+
+
+@pytest.mark.parametrize("hkv", [2, 1])
+def test_bad_positions_clamped_on_a_linear_cache_of_many_chunks(wa, hkv):
+    """Out-of-range positions on the tensor-core path (groups of 4 and 8, 16 chunks a row): reported,
+    and the rows computed as at the clamped positions."""
+    c = _case(3, 8, hkv, 128, 0, 4096, [0, 4095, 100], seed=15, outside="keep")
+    ws = torch.empty(wa.decode_ws_bytes(3, 8, 128, 0, 4096), dtype=torch.uint8, device="cuda")
+    bad = torch.tensor([-3, 7000, 100], dtype=torch.int32, device="cuda")
+    out = wa.decode(c["q"], c["k"], c["v"], bad, 0, 1.0, ws=ws)
+    assert wa.status(ws) & wa.WA_STATUS_BAD_POS
+    clamped = wa.decode(c["q"], c["k"], c["v"], c["pos"], 0, 1.0, ws=ws)
+    assert wa.status(ws) == 0
+    assert torch.equal(out.view(torch.int16), clamped.view(torch.int16))
+
+
+def test_linear_cache_past_the_sorted_schedule(wa):
+    """A linear cache of 1,026 chunks a row: too many for the tensor-core decode's sorted schedule,
+    so its units go out in a plain stride."""
+    ring = 1025 * 256 + 44
+    c = _case(2, 8, 1, 128, 0, ring, [ring - 1, 5000], seed=16)
+    out = wa.decode(c["q"], c["k"], c["v"], c["pos"], 0, 1.0)
+    assert_parity(out, decode_ref(c), TOL, "stride schedule")
 
 
 def test_bad_positions_are_clamped_and_reported(wa):
