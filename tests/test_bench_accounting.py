@@ -90,3 +90,31 @@ def test_part_report_fractions_use_the_burst_peak():
     r = bench.report_part("prompt_causal", ms, pk)
     assert np.isclose(r["TFLOP/s"], 1000.0)
     assert np.isclose(r["frac_bf16"], 0.5) and np.isclose(r["frac_bf16_sustained"], 0.625)
+
+
+def _flow_shop_span(order, first, second):
+    """Span of jobs through two machines in series, each job's second stage after its first."""
+    t1 = t2 = 0.0
+    for i in order:
+        t1 += first[i]
+        t2 = max(t2, t1) + second[i]
+    return t2
+
+
+def test_e2e_part_order_is_a_shortest_two_stage_schedule():
+    """The e2e leg issues the parts' copies in Johnson's order; by brute force over every order of
+    small random instances, that order reaches the shortest two-machine span."""
+    import itertools
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        n = int(rng.integers(1, 7))
+        first = list(rng.uniform(0.1, 10.0, n))
+        second = list(rng.uniform(0.1, 10.0, n))
+        best = min(_flow_shop_span(p, first, second) for p in itertools.permutations(range(n)))
+        got = bench.johnson_order(first, second)
+        assert sorted(got) == list(range(n))
+        assert _flow_shop_span(got, first, second) <= best * (1 + 1e-12)
+    # the default step's shape: dense prompts (short copies, long kernels) first, then the cache
+    # parts by kernel time
+    order = bench.johnson_order([7.6, 7.6, 0.7, 11.4, 161.0], [38.0, 28.0, 0.5, 0.6, 3.7])
+    assert order == [0, 1, 4, 3, 2]
