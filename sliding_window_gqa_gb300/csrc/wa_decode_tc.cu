@@ -52,7 +52,8 @@ namespace {
 constexpr int kSub = 64;          // keys per sub-tile
 constexpr int kTcThreads = 160;
 constexpr int kUnitSlots = 8;     // units published ahead of the slowest role
-constexpr int kPlanRows = 4096;      // the sorted schedule serves calls up to this many rows ...
+constexpr int kUnitAhead = 4;     // units the producer publishes beyond the one it loads
+constexpr int kPlanRows = 2048;      // the sorted schedule serves calls up to this many rows ...
 constexpr int kPlanChunks = 1024;    // ... and chunks a row; larger calls take units in a plain stride
 constexpr float kLazyTc = 8.0f;   // log2 units the running max may trail before O is rescaled
 
@@ -99,7 +100,8 @@ struct TcCfg {
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;    // [0] tensor-memory base
     static constexpr int OFF_RING = OFF_MISC + 16;         // kUnitSlots units (8 ints each)
     static constexpr int OFF_PERM = OFF_RING + 32 * kUnitSlots;  // kPlanRows: row | chunks << 16, by chunks, descending
-    static constexpr int OFF_CUR = OFF_PERM + 4 * kPlanRows;     // kPlanChunks + 1: histogram, then sort cursors
+    static constexpr int OFF_POS = OFF_PERM + 4 * kPlanRows;     // kPlanRows: clamped positions
+    static constexpr int OFF_CUR = OFF_POS + 4 * kPlanRows;      // kPlanChunks + 1: histogram, then sort cursors
     static constexpr int OFF_ACC = OFF_CUR + 4 * (kPlanChunks + 1);     // kPlanChunks: rows in level 0, 1, ...
     static constexpr int OFF_START = OFF_ACC + 4 * kPlanChunks;          // kPlanChunks + 1: first unit of each level
     static constexpr int SMEM = OFF_START + 4 * (kPlanChunks + 1);
@@ -141,21 +143,19 @@ struct Unit {
     int r, g, ci, cbase, kb, ke, t0, nt;
 };
 
-// Fills x for unit index u = (r * hkv + g) * cmax + ci; false when the chunk
-// holds none of the row's keys.  Out-of-range positions are clamped (and
-// reported once per row by the caller that passes report).
-__device__ __forceinline__ bool unit_at(const TcParams& p, int u, Unit& x, bool report) {
-    x.ci = u % p.cmax;
-    const int rg = u / p.cmax;
-    x.g = rg % p.hkv;
-    x.r = rg / p.hkv;
-    int pp = p.pos[x.r];
-    if (pp < 0 || (p.win == 0 && pp >= p.ring)) {
-        if (report && x.ci == 0 && x.g == 0) atomicOr(p.status, WA_STATUS_BAD_POS);
-        pp = pp < 0 ? 0 : p.ring - 1;
-    }
+// A decode position as the kernels use it: out-of-range positions clamped (the caller reports).
+__device__ __forceinline__ int clamp_pos(const TcParams& p, int pp) {
+    return (pp < 0 || (p.win == 0 && pp >= p.ring)) ? (pp < 0 ? 0 : p.ring - 1) : pp;
+}
+
+// Fills x for row r, key head g and chunk ci of a row at clamped position pp; false when the
+// chunk holds none of the row's keys.
+__device__ __forceinline__ bool unit_from(const TcParams& p, int r, int g, int ci, int pp, Unit& x) {
+    x.r = r;
+    x.g = g;
+    x.ci = ci;
     const int lo = p.win > 0 ? max(0, pp - p.win + 1) : 0;
-    const int c = lo / kChunk + x.ci;
+    const int c = lo / kChunk + ci;
     if (c > pp / kChunk) return false;
     x.cbase = c * kChunk;
     x.kb = max(lo, x.cbase);
@@ -165,10 +165,19 @@ __device__ __forceinline__ bool unit_at(const TcParams& p, int u, Unit& x, bool 
     return true;
 }
 
-// Chunks holding any of row r's keys (at least 1), with unit_at's clamping.
-__device__ __forceinline__ int row_chunks(const TcParams& p, int r) {
-    int pp = p.pos[r];
-    if (pp < 0 || (p.win == 0 && pp >= p.ring)) pp = pp < 0 ? 0 : p.ring - 1;
+// The same for unit index u = (r * hkv + g) * cmax + ci, reading the row's position (reported once
+// per row, by its unit (r, 0, 0), when out of range).
+__device__ __forceinline__ bool unit_at(const TcParams& p, int u, Unit& x, bool report) {
+    const int ci = u % p.cmax, rg = u / p.cmax;
+    const int g = rg % p.hkv, r = rg / p.hkv;
+    const int raw = p.pos[r];
+    const int pp = clamp_pos(p, raw);
+    if (report && pp != raw && ci == 0 && g == 0) atomicOr(p.status, WA_STATUS_BAD_POS);
+    return unit_from(p, r, g, ci, pp, x);
+}
+
+// Chunks holding any of a row's keys (at least 1) at clamped position pp.
+__device__ __forceinline__ int chunks_at(const TcParams& p, int pp) {
     const int lo = p.win > 0 ? max(0, pp - p.win + 1) : 0;
     return min(p.cmax, pp / kChunk - lo / kChunk + 1);
 }
@@ -235,6 +244,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
             prefetch_tensormap(&p.tv);
         }
         uint32_t* perm = reinterpret_cast<uint32_t*>(smem + C::OFF_PERM);
+        int* spos = reinterpret_cast<int*>(smem + C::OFF_POS);
         int* cur = reinterpret_cast<int*>(smem + C::OFF_CUR);
         int* acc = reinterpret_cast<int*>(smem + C::OFF_ACC);
         int* start = reinterpret_cast<int*>(smem + C::OFF_START);
@@ -245,7 +255,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
             // rows sorted by chunk count, descending (counting sort)
             for (int c = lane; c <= cm; c += 32) cur[c] = 0;
             __syncwarp();
-            for (int r = lane; r < p.rows; r += 32) atomicAdd(&cur[row_chunks(p, r)], 1);
+            for (int r = lane; r < p.rows; r += 32) {
+                const int raw = p.pos[r];
+                const int pp = clamp_pos(p, raw);
+                if (pp != raw && blockIdx.x == 0) atomicOr(p.status, WA_STATUS_BAD_POS);
+                spos[r] = pp;
+                atomicAdd(&cur[chunks_at(p, pp)], 1);
+            }
             __syncwarp();
             // level l takes the chunk e = cm - 1 - l places from each row's end; acc[l] = rows with more than e chunks
             int carry = 0;
@@ -270,14 +286,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
             for (int c = lane; c <= cm; c += 32) cur[c] = c >= cm ? 0 : acc[cm - 1 - c];
             __syncwarp();
             for (int r = lane; r < p.rows; r += 32) {
-                const int n = row_chunks(p, r);
+                const int n = chunks_at(p, spos[r]);
                 perm[atomicAdd(&cur[n], 1)] = static_cast<uint32_t>(r) | (static_cast<uint32_t>(n) << 16);
             }
             __syncwarp();
             total = start[cm];
         }
         // unit k of the schedule: the row's chunks from its end are last, first, then the middle ones
-        auto unit_of = [&](int k) -> int {
+        auto unit_of = [&](int k, Unit& x) {
             int lo = 0, hi = cm - 1;
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
@@ -288,23 +304,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
             const int r = static_cast<int>(ent & 0xFFFFu), n = static_cast<int>(ent >> 16), g = j % p.hkv;
             const int rank = n - 1 - e;
             const int ci = rank == n - 1 ? n - 1 : (rank == n - 2 ? 0 : rank + 1);
-            return (r * p.hkv + g) * cm + ci;
+            unit_from(p, r, g, ci, spos[r], x);
         };
-        // A CTA's first unit is its index; each later one comes from the counter, asked one unit
-        // ahead so its answer is back before it is needed.  Without a schedule: a plain stride.
+        // The next unit (x.nt = 0 once there is none).  A CTA's first unit is its index; each later
+        // one comes from the counter, asked one unit ahead so its answer is back before it is
+        // needed.  Without a schedule: a plain stride, skipping empty chunks.
         int k_cur = blockIdx.x, k_ans = 0, su = blockIdx.x;
         bool asked = false;
-        auto next_unit = [&]() -> int {
+        auto next_unit = [&](Unit& x) {
+            x = Unit{};
             if (planned) {
                 if (asked) k_cur = __shfl_sync(0xFFFFFFFFu, k_ans, 0) + static_cast<int>(gridDim.x);
-                if (k_cur >= total) return -1;
+                if (k_cur >= total) return;
                 if (lane == 0) k_ans = atomicAdd(p.next_unit, 1);
                 asked = true;
-                return unit_of(k_cur);
+                unit_of(k_cur, x);
+                return;
             }
-            const int u = su < units ? su : -1;
-            su += gridDim.x;
-            return u;
+            for (; su < units; su += gridDim.x)
+                if (unit_at(p, su, x, lane == 0)) {
+                    su += gridDim.x;
+                    return;
+                }
+            x = Unit{};
         };
         int Upub = 0;
         auto publish = [&](const Unit& x) -> bool {
@@ -322,19 +344,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
             ++Upub;
             return true;
         };
+        // publish the next unit, or the end marker once (x.nt = 0)
+        bool ended = false;
+        auto publish_next = [&]() -> bool {
+            if (ended) return true;
+            Unit x;
+            next_unit(x);
+            ended = x.nt <= 0;
+            return publish(x);
+        };
         const size_t row_elems = static_cast<size_t>(p.ring) * p.hkv * D;
         bool ok = true;
         int issued[2] = {0, 0};
         int T = 0;
-        while (ok) {
-            const int u = next_unit();
-            Unit x{};
-            if (u >= 0 && !unit_at(p, u, x, lane == 0)) continue;   // an empty chunk (stride only)
-            if (!publish(x)) {   // x.nt = 0: the end
-                ok = false;
-                break;
+        // The producer keeps kUnitAhead units published beyond the one it loads, so every role
+        // knows its next unit (and the Q/O warp can fetch its queries) well before it starts.
+        for (int l = 0; l < kUnitAhead && ok; ++l) ok = publish_next();
+        for (int U = 0; ok; ++U) {
+            Unit x;
+            {
+                volatile int* e = uring + 8 * (U % kUnitSlots);   // published by this warp
+                x.r = e[0]; x.g = e[1]; x.ci = e[2]; x.cbase = e[3];
+                x.kb = e[4]; x.ke = e[5]; x.t0 = e[6]; x.nt = e[7];
             }
-            if (u < 0) break;
+            if (x.nt <= 0) break;
+            if (!(ok = publish_next())) break;
             for (int idx = 0; idx < x.nt && ok; ++idx, ++T) {
                 const int key0 = x.cbase + (x.t0 + idx) * kSub;
                 const int slot0 = key0 % p.ring;
