@@ -190,6 +190,17 @@ def test_linear_cache_past_the_sorted_schedule(wa):
     assert_parity(out, decode_ref(c), TOL, "stride schedule")
 
 
+def test_many_rows_past_the_sorted_schedule(wa):
+    """2,100 rows at groups of 4: more rows than the tensor-core decode's sorted schedule holds, so
+    its units go out in a plain stride; sampled rows against the oracle."""
+    gen = torch.Generator().manual_seed(17)
+    pos = torch.randint(0, 5000, (2100,), generator=gen).tolist()
+    c = _case(2100, 4, 1, 128, 64, 64, pos, seed=17, outside="keep")
+    out = wa.decode(c["q"], c["k"], c["v"], c["pos"], 64, 1.0)
+    rows = [0, 1, 777, 2047, 2048, 2099]
+    assert_parity(out[rows], decode_ref(c, rows=rows), TOL, "stride schedule, many rows")
+
+
 def test_bad_positions_are_clamped_and_reported(wa):
     c = _case(2, 4, 2, 128, 0, 512, [10, 20], seed=13, outside="keep")
     ws = torch.empty(wa.decode_ws_bytes(2, 4, 128, 0, 512), dtype=torch.uint8, device="cuda")
