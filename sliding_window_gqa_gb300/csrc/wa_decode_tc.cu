@@ -49,13 +49,13 @@ namespace wa {
 
 namespace {
 
-constexpr int kSub = 64;          // keys per sub-tile
+constexpr int kSub = 64;            // keys per sub-tile
 constexpr int kTcThreads = 160;
-constexpr int kUnitSlots = 8;     // units published ahead of the slowest role
-constexpr int kUnitAhead = 4;     // units the producer publishes beyond the one it loads
-constexpr int kPlanRows = 2048;      // the sorted schedule serves calls up to this many rows ...
-constexpr int kPlanChunks = 1024;    // ... and chunks a row; larger calls take units in a plain stride
-constexpr float kLazyTc = 8.0f;   // log2 units the running max may trail before O is rescaled
+constexpr int kUnitSlots = 8;       // unit slots: published units not yet taken by every role
+constexpr int kUnitAhead = 4;       // units the producer publishes beyond the one it loads
+constexpr int kPlanRows = 2048;     // the sorted schedule serves calls up to this many rows ...
+constexpr int kPlanChunks = 1024;   // ... and chunks a row; larger calls take units in a plain stride
+constexpr float kLazyTc = 8.0f;     // log2 units the running max may trail before O is rescaled
 
 struct TcParams {
     CUtensorMap tk, tv;           // [rows][ring][hkv][d] rings, box 64 x 1 x 64 x 1, 128-byte swizzle
