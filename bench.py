@@ -999,7 +999,7 @@ def main():
     ap.add_argument("--no-next", action="store_true", help="same as --next none")
     ap.add_argument("--oracle-one-core", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=6, help="e2e steps timed (the host link's rate varies from copy to copy; the mean over these)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=4.0, help="oracle seconds per reference step")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="oracle seconds for cpu_baseline")
