@@ -69,6 +69,14 @@ CASES = [
     ("d256_gqa16_bf16", 150, 100, 16, 1, 256, 128, 256, [], False),
     ("d256_gqa3", 129, 4000, 6, 2, 256, 1024, 1536, [(120, 128)], True),
     ("window_1", 130, 40, 2, 1, 128, 1, 256, [], True),
+    # head dim 128 with P32 (two query tiles a CTA): causal, ring-wrap copies, image spans, and a
+    # call whose one pair of tiles has no second tile
+    ("d128_linear_causal_700_p32", 700, 0, 8, 4, 128, 0, 700, [], True),
+    ("d128_wrapcopy_p32", 300, 2000, 8, 4, 128, 500, 1000, [(10, 60)], True),
+    ("d128_chunk512_p1300_image_p32", 512, 1300, 16, 8, 128, 1024, 1536, [(40, 300)], True),
+    ("d128_one_tile_n100_p32", 100, 3000, 4, 2, 128, 1024, 1536, [], True),
+    ("d128_one_tile_n100_bf16", 100, 3000, 4, 2, 128, 1024, 1536, [], False),
+    ("linear_causal_700_bf16", 700, 0, 16, 8, 256, 0, 700, [], False),
 ]
 
 
